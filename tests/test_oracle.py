@@ -1,0 +1,356 @@
+"""Pins of the fp64 CPU oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each test checks it against a worked
+example printed on a page (tests/golden/), a different formulation printed on a
+page (the HF diagonal formulas, the torch_sdpa tril/triu window), a library routine
+(torch scaled_dot_product_attention in fp64), a closed form, or an invariant that a
+plausible slip (dropped scale, wrong GQA mapping, wrong block/offset split, top-left
+instead of bottom-right causal alignment, off-by-one window) would break.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_03_gb300.inputs import (SMALL_WORKLOADS, Workload, bf16_bits,
+                                                make_case, make_case_from_lengths)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden_mask(name):
+    rows, header = [], None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if header is None:
+                header = dict(kv.split("=") for kv in line.split())
+                continue
+            rows.append([c == "1" for c in line])
+    return int(header["sk"]), int(header["sq"]), int(header["window"]), np.array(rows)
+
+
+# ------------------------------------------------------------------ masks ---
+
+@pytest.mark.parametrize("name", ["hf_mask_example_1.txt", "hf_mask_example_2.txt"])
+def test_mask_matches_printed_examples(name):
+    sk, sq, w, expect = _read_golden_mask(name)
+    got = oracle.mask(sq, sk, w)
+    assert got.shape == expect.shape
+    np.testing.assert_array_equal(got, expect)
+
+
+def _hf_formula_allowed(sq, sk, w):
+    """build_attention_mask's diagonals ("transformers ... input_ouputs.py"), as printed:
+    causal diagonal sk - sq + 1 when 1 <= sq < sk (else 1), triu of -inf above it; if
+    w > 1 also tril of -inf at diagonal sk - sq - w."""
+    causal_diagonal = sk - sq + 1 if 1 <= sq < sk else 1
+    ones = torch.ones(sq, sk, dtype=torch.bool)
+    masked = torch.triu(ones, diagonal=causal_diagonal)
+    if w > 1:
+        masked |= torch.tril(ones, diagonal=sk - sq - w)
+    return (~masked).numpy()
+
+
+@pytest.mark.parametrize("w", [0, 2, 3, 5, 8, 100])
+def test_mask_matches_hf_diagonal_formulas(w):
+    for sk in range(1, 14):
+        for sq in range(1, sk + 1):
+            np.testing.assert_array_equal(oracle.mask(sq, sk, w), _hf_formula_allowed(sq, sk, w),
+                                          err_msg=f"sq={sq} sk={sk} w={w}")
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 7, 20])
+def test_square_window_matches_sdpa_bias(w):
+    # torch_sdpa.py _make_sliding_window_bias: tril(ones, 0) then triu(., -w + 1).
+    for n in range(1, 12):
+        keep = torch.triu(torch.tril(torch.ones(n, n), diagonal=0), diagonal=-w + 1) > 0
+        np.testing.assert_array_equal(oracle.mask(n, n, w), keep.numpy())
+
+
+def test_window_one_is_self_only_and_rejects_more_queries_than_keys():
+    np.testing.assert_array_equal(oracle.mask(3, 6, 1),
+                                  np.array([[0, 0, 0, 1, 0, 0], [0, 0, 0, 0, 1, 0],
+                                            [0, 0, 0, 0, 0, 1]], dtype=bool))
+    with pytest.raises(oracle.OracleError):
+        oracle.mask(4, 3, 0)
+
+
+# ------------------------------------------------------------------ store ---
+
+def test_store_matches_printed_example():
+    with open(os.path.join(GOLDEN, "store_kvcache_example.txt")) as f:
+        lines = [l.strip() for l in f if l.strip() and not l.startswith("#")]
+    hdr = dict(kv.split("=") for kv in lines[0].split())
+    T, hkv, d = int(hdr["num_tokens"]), int(hdr["num_kv_heads"]), int(hdr["head_dim"])
+    nb, bs = int(hdr["num_blocks"]), int(hdr["block_size"])
+    slots = np.array([int(x) for x in lines[1].split("=")[1].split(",")], dtype=np.int32)
+    where = {int(a): int(b) for a, b in (l.split() for l in lines[2:])}
+    g = torch.Generator().manual_seed(7)
+    key = bf16_bits(torch.randn(T, hkv, d, generator=g).to(torch.bfloat16))
+    value = bf16_bits(torch.randn(T, hkv, d, generator=g).to(torch.bfloat16))
+    kc = np.zeros((nb, bs, hkv, d), np.uint16)
+    vc = np.zeros((nb, bs, hkv, d), np.uint16)
+    oracle.store_kvcache(key, value, kc, vc, slots, bs)
+    flat_k, flat_v = kc.reshape(nb * bs, hkv, d), vc.reshape(nb * bs, hkv, d)
+    written = set()
+    for t, s in where.items():
+        if s < 0:
+            continue
+        np.testing.assert_array_equal(flat_k[s], key[t])
+        np.testing.assert_array_equal(flat_v[s], value[t])
+        written.add(s)
+    untouched = [s for s in range(nb * bs) if s not in written]
+    assert not flat_k[untouched].any() and not flat_v[untouched].any()
+    # slot 16 is block 1, row 0 of the [num_blocks, block_size, ...] cache
+    np.testing.assert_array_equal(kc[1, 0], key[2])
+
+
+def test_store_random_slots_matches_numpy_scatter():
+    rng = np.random.default_rng(3)
+    nb, bs, hkv, d, T = 12, 16, 4, 64, 70
+    slots = rng.permutation(nb * bs)[:T].astype(np.int32)
+    slots[rng.random(T) < 0.2] = -1
+    key = rng.integers(0, 1 << 16, (T, hkv, d), dtype=np.uint16)
+    value = rng.integers(0, 1 << 16, (T, hkv, d), dtype=np.uint16)
+    kc0 = rng.integers(0, 1 << 16, (nb, bs, hkv, d), dtype=np.uint16)
+    vc0 = rng.integers(0, 1 << 16, (nb, bs, hkv, d), dtype=np.uint16)
+    kc, vc = kc0.copy(), vc0.copy()
+    oracle.store_kvcache(key, value, kc, vc, slots, bs)
+    ek, ev = kc0.reshape(nb * bs, hkv, d).copy(), vc0.reshape(nb * bs, hkv, d).copy()
+    keep = slots >= 0
+    ek[slots[keep]] = key[keep]
+    ev[slots[keep]] = value[keep]
+    np.testing.assert_array_equal(kc.reshape(nb * bs, hkv, d), ek)
+    np.testing.assert_array_equal(vc.reshape(nb * bs, hkv, d), ev)
+
+
+def test_store_rejects_slot_past_the_pool():
+    kc = np.zeros((2, 16, 1, 8), np.uint16)
+    with pytest.raises(oracle.OracleError):
+        oracle.store_kvcache(np.zeros((1, 1, 8), np.uint16), np.zeros((1, 1, 8), np.uint16),
+                             kc, kc.copy(), np.array([32], np.int32), 16)
+
+
+def test_bf16_widening_is_exact():
+    for bits, val in ((0x3F80, 1.0), (0xC000, -2.0), (0x3E80, 0.25), (0x0000, 0.0),
+                      (0x7F80, math.inf)):
+        assert oracle.bf16_to_double(bits) == val
+
+
+# -------------------------------------------------------------- attention ---
+
+def _contiguous_case(H, Hkv, D, ctx, ql, window=0, bs=16, seed=0):
+    """A case whose block tables are the identity (sequence i owns consecutive blocks
+    in pool order), so the paged cache read equals a contiguous K/V per sequence."""
+    w = Workload("pin", H, Hkv, D, bs, (), sliding_window=window)
+    case = make_case_from_lengths(w, ctx, ql, seed=seed)
+    nblk = (case.seq_lens + bs - 1) // bs
+    bt = np.full_like(case.block_table, -1)
+    c = 0
+    for i, n in enumerate(nblk):
+        bt[i, :n] = np.arange(c, c + n)
+        c += n
+    case.block_table = bt
+    return case
+
+
+def _run_oracle(case, window=None, num_threads=0):
+    w = case.workload
+    return oracle.paged_attention(bf16_bits(case.q), bf16_bits(case.k_cache),
+                                  bf16_bits(case.v_cache), case.cu_seqlens_q, case.seq_lens,
+                                  case.block_table, w.num_heads, w.num_kv_heads,
+                                  w.sliding_window if window is None else window,
+                                  w.final_scale, num_threads)
+
+
+def _contiguous_kv(case, i):
+    """K, V [sk, Hkv, D] float64 of sequence i read straight from the pool order."""
+    bs = case.workload.block_size
+    sk = int(case.seq_lens[i])
+    blocks = case.block_table[i, :(sk + bs - 1) // bs]
+    k = case.k_cache.double()[torch.as_tensor(blocks, dtype=torch.long)].reshape(
+        -1, case.workload.num_kv_heads, case.workload.head_dim)[:sk]
+    v = case.v_cache.double()[torch.as_tensor(blocks, dtype=torch.long)].reshape(
+        -1, case.workload.num_kv_heads, case.workload.head_dim)[:sk]
+    return k, v
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (10, 2)])
+def test_prefill_equals_torch_sdpa_causal(H, Hkv):
+    # torch_sdpa.py prompt path: per-sequence scaled_dot_product_attention with
+    # is_causal and K/V repeat_interleave'd by num_queries_per_kv.
+    case = _contiguous_case(H, Hkv, 32, [0, 0, 0], [5, 17, 33], seed=1)
+    got = _run_oracle(case)
+    G = H // Hkv
+    for i in range(case.num_seqs):
+        a, b = case.cu_seqlens_q[i], case.cu_seqlens_q[i + 1]
+        q = case.q[a:b].double().transpose(0, 1)
+        k, v = _contiguous_kv(case, i)
+        k = k.repeat_interleave(G, dim=1).transpose(0, 1)
+        v = v.repeat_interleave(G, dim=1).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, is_causal=True, scale=case.workload.final_scale).transpose(0, 1)
+        np.testing.assert_allclose(got[a:b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [0, 1, 3, 16, 40])
+def test_chunked_prefill_equals_sdpa_with_hf_mask(window):
+    case = _contiguous_case(8, 2, 64, [0, 9, 30, 47], [6, 7, 1, 20], window=window, seed=2)
+    got = _run_oracle(case)
+    for i in range(case.num_seqs):
+        a, b = case.cu_seqlens_q[i], case.cu_seqlens_q[i + 1]
+        sq, sk = b - a, int(case.seq_lens[i])
+        if window == 1:  # HF spells "no window" as 1; the square sdpa formula covers w = 1
+            ones = torch.ones(sq, sk)
+            allowed = torch.zeros(sq, sk, dtype=torch.bool)
+            for r in range(sq):
+                allowed[r, sk - sq + r] = True
+        else:
+            allowed = torch.as_tensor(_hf_formula_allowed(sq, sk, window))
+        q = case.q[a:b].double().transpose(0, 1)
+        k, v = _contiguous_kv(case, i)
+        k = k.repeat_interleave(4, dim=1).transpose(0, 1)
+        v = v.repeat_interleave(4, dim=1).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, attn_mask=allowed, scale=case.workload.final_scale).transpose(0, 1)
+        np.testing.assert_allclose(got[a:b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_block_table_permutation_invariance():
+    case = make_case("batched_decode_small", seed=5)
+    base = _run_oracle(case)
+    rng = np.random.default_rng(0)
+    nb = case.num_blocks
+    perm = rng.permutation(nb)  # new physical index of old block b is perm[b]
+    kc = torch.empty_like(case.k_cache)
+    vc = torch.empty_like(case.v_cache)
+    kc[torch.as_tensor(perm)] = case.k_cache
+    vc[torch.as_tensor(perm)] = case.v_cache
+    bt = np.where(case.block_table >= 0, perm[np.maximum(case.block_table, 0)], -1)
+    case.k_cache, case.v_cache, case.block_table = kc, vc, bt.astype(np.int32)
+    np.testing.assert_array_equal(_run_oracle(case), base)
+
+
+def test_constant_v_gives_v():
+    case = make_case("mixed_window_small", seed=6)
+    row = torch.randn(case.workload.num_kv_heads, case.workload.head_dim).to(torch.bfloat16)
+    case.v_cache[:] = row
+    got = _run_oracle(case)
+    G = case.workload.num_heads // case.workload.num_kv_heads
+    expect = row.double().repeat_interleave(G, dim=0).numpy()
+    np.testing.assert_allclose(got, np.broadcast_to(expect, got.shape), rtol=0, atol=1e-12)
+
+
+def test_zero_query_gives_mean_of_visible_values():
+    # q = 0 -> every visible logit is 0 -> uniform weights (closed form).
+    case = make_case("mixed_window_small", seed=8)
+    case.q.zero_()
+    got = _run_oracle(case)
+    w = case.workload
+    G = w.num_heads // w.num_kv_heads
+    for i in range(case.num_seqs):
+        k, v = _contiguous_kv_any(case, i)
+        a = case.cu_seqlens_q[i]
+        sq, sk = case.query_lens[i], case.seq_lens[i]
+        for r in (0, sq - 1):
+            p = sk - sq + r
+            lo = max(0, p - w.sliding_window + 1) if w.sliding_window > 0 else 0
+            mean = v[lo:p + 1].mean(0)
+            np.testing.assert_allclose(got[a + r], mean.repeat_interleave(G, 0).numpy(),
+                                       rtol=0, atol=1e-12)
+
+
+def _contiguous_kv_any(case, i):
+    bs = case.workload.block_size
+    sk = int(case.seq_lens[i])
+    idx = torch.as_tensor(case.block_table[i, :(sk + bs - 1) // bs], dtype=torch.long)
+    shp = (-1, case.workload.num_kv_heads, case.workload.head_dim)
+    return (case.k_cache.double()[idx].reshape(shp)[:sk],
+            case.v_cache.double()[idx].reshape(shp)[:sk])
+
+
+def test_decode_equals_last_row_of_full_prefill():
+    w = Workload("pin", 8, 2, 64, 16, ())
+    lens = [1, 16, 17, 50]
+    pre = make_case_from_lengths(w, [0] * 4, lens, seed=9)
+    full = _run_oracle(pre)
+    dec = make_case_from_lengths(w, [n - 1 for n in lens], [1] * 4, seed=9)
+    dec.k_cache, dec.v_cache, dec.block_table = pre.k_cache, pre.v_cache, pre.block_table
+    dec.q = pre.q[torch.as_tensor(pre.cu_seqlens_q[1:] - 1, dtype=torch.long)]
+    got = _run_oracle(dec)
+    np.testing.assert_array_equal(got, full[pre.cu_seqlens_q[1:] - 1])
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    case = make_case("mixed_window_small", seed=10)
+    gqa = _run_oracle(case)
+    w = case.workload
+    G = w.num_heads // w.num_kv_heads
+    mha_w = Workload("mha", w.num_heads, w.num_heads, w.head_dim, w.block_size, (),
+                     sliding_window=w.sliding_window)
+    mha = make_case_from_lengths(mha_w, case.context_lens, case.query_lens, seed=10)
+    mha.q = case.q
+    mha.block_table = case.block_table
+    mha.k_cache = case.k_cache.repeat_interleave(G, dim=2).contiguous()
+    mha.v_cache = case.v_cache.repeat_interleave(G, dim=2).contiguous()
+    np.testing.assert_array_equal(_run_oracle(mha), gqa)
+
+
+def test_window_at_least_seq_len_is_no_window_and_window_one_is_own_value():
+    case = make_case("mixed_window_small", seed=11)
+    big = int(case.seq_lens.max())
+    np.testing.assert_array_equal(_run_oracle(case, window=big), _run_oracle(case, window=0))
+    got = _run_oracle(case, window=1)
+    w = case.workload
+    G = w.num_heads // w.num_kv_heads
+    for i in range(case.num_seqs):
+        _, v = _contiguous_kv_any(case, i)
+        a = case.cu_seqlens_q[i]
+        sq, sk = case.query_lens[i], case.seq_lens[i]
+        for r in range(sq):
+            np.testing.assert_array_equal(
+                got[a + r], v[sk - sq + r].repeat_interleave(G, 0).numpy())
+
+
+def test_brute_force_tiny_against_hand_softmax():
+    # Two keys, one head: o = (e^{s0} v0 + e^{s1} v1) / (e^{s0} + e^{s1}).
+    w = Workload("pin", 1, 1, 8, 1, (), scale=0.5)
+    case = make_case_from_lengths(w, [1], [1], seed=12)
+    got = _run_oracle(case)[0, 0]
+    q = case.q.double()[0, 0]
+    ks = [case.k_cache.double()[case.block_table[0, j], 0, 0] for j in range(2)]
+    vs = [case.v_cache.double()[case.block_table[0, j], 0, 0] for j in range(2)]
+    s = [0.5 * float(q @ k) for k in ks]
+    e = [math.exp(x) for x in s]
+    expect = (e[0] * vs[0] + e[1] * vs[1]) / (e[0] + e[1])
+    np.testing.assert_allclose(got, expect.numpy(), rtol=1e-14, atol=1e-14)
+
+
+def test_empty_sequence_gives_zero_row_and_bad_block_is_reported():
+    w = Workload("pin", 2, 1, 16, 16, ())
+    case = make_case_from_lengths(w, [0, 3], [0, 1], seed=13)
+    # decode-style call with an empty first sequence
+    out = oracle.paged_attention(bf16_bits(case.q), bf16_bits(case.k_cache),
+                                 bf16_bits(case.v_cache), np.array([0, 0, 1], np.int32),
+                                 case.seq_lens, case.block_table, 2, 1, 0, 0.25)
+    assert out.shape[0] == 1
+    bad = case.block_table.copy()
+    bad[1, 0] = case.num_blocks + 5
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_attention(bf16_bits(case.q), bf16_bits(case.k_cache),
+                               bf16_bits(case.v_cache), case.cu_seqlens_q, case.seq_lens, bad,
+                               2, 1, 0, 0.25)
+    row = oracle.attend_row(bf16_bits(case.q[0]), bf16_bits(case.k_cache),
+                            bf16_bits(case.v_cache), case.block_table[0], 0, 0, 2, 1, 0, 0.25)
+    assert not row.any()
+
+
+def test_thread_count_does_not_change_result():
+    case = make_case("varlen_prefill_small", seed=14)
+    np.testing.assert_array_equal(_run_oracle(case, num_threads=1), _run_oracle(case, num_threads=5))
