@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention hot path on GB300.
+
+Default workload: batched decode, Llama-3-8B-shaped layer (32 query / 8 kv heads,
+head_dim 128, block_size 16, 32768-block pool, batch 64, seq_len U[512, 4096]).  One
+step = store the 64 new tokens' K/V through slot_mapping, then split-K paged decode
+and the LSE combine (one pa_decode call with the fused store).  The metric is decode
+KV-read GB/s: the K and V bytes the attention must read (sum over sequences of the
+attended keys x num_kv_heads x head_dim x 2 tensors x 2 bytes) divided by the step
+time.  A second leg times the varlen causal prefill workload (16 prompts of
+U[128, 2048] tokens, store + prefill) in TFLOP/s (4 x head_dim x num_heads FLOP per
+unmasked query/key pair).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_attention_03_gb300.inputs import WORKLOADS, make_case, split_mixed  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, ws
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ work counting ---
+
+def attended_keys(case, seqs=None):
+    """Per query row, the number of visible keys (bottom-right causal + window)."""
+    w = case.workload.sliding_window
+    seqs = range(case.num_seqs) if seqs is None else seqs
+    total = 0
+    for i in seqs:
+        sq, sk = int(case.query_lens[i]), int(case.seq_lens[i])
+        p = np.arange(sk - sq, sk, dtype=np.int64)
+        n = p + 1
+        if w > 0:
+            n = np.minimum(n, w)
+        total += int(n.sum())
+    return total
+
+
+def decode_kv_bytes(case, seqs=None):
+    """K+V bytes decode must read: attended keys x Hkv x D x 2 tensors x 2 bytes."""
+    w = case.workload
+    return attended_keys(case, seqs) * w.num_kv_heads * w.head_dim * 2 * 2
+
+
+def prefill_flops(case, seqs=None):
+    w = case.workload
+    return attended_keys(case, seqs) * 4 * w.head_dim * w.num_heads
+
+
+# ------------------------------------------------------------------ runners ---
+
+class DecodeRunner:
+    """One step: fused store of the new tokens + split-K decode (+ combine)."""
+
+    def __init__(self, case, device, seqs=None):
+        import paged_kv_attention_03_gb300 as pa
+
+        self.pa = pa
+        self.case = case
+        w = case.workload
+        self.seqs = np.arange(case.num_seqs) if seqs is None else np.asarray(seqs)
+        t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=device)
+        rows = torch.as_tensor(case.cu_seqlens_q[self.seqs], dtype=torch.long, device=device)
+        self.q = case.q[rows].contiguous()
+        self.key = case.key[rows].contiguous()
+        self.value = case.value[rows].contiguous()
+        self.slots = t(case.slot_mapping[case.cu_seqlens_q[self.seqs]])
+        self.bt = t(case.block_table[self.seqs])
+        self.seq_lens = t(case.seq_lens[self.seqs])
+        self.max_len = int(case.seq_lens[self.seqs].max())
+        self.window = w.sliding_window
+        self.scale = w.final_scale
+        self.out = torch.empty_like(self.q)
+        self.splits = pa.pa_decode_num_splits(len(self.seqs), w.num_heads, w.num_kv_heads,
+                                              w.head_dim, self.max_len, self.window, 0)
+        need = pa.pa_decode_workspace_size(len(self.seqs), w.num_heads, w.num_kv_heads,
+                                           w.head_dim, self.max_len, self.window, 0)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.launches = 2 + (1 if self.splits > 1 else 0)
+        self.work = decode_kv_bytes(case, self.seqs)
+
+    def step(self):
+        self.pa.pa_decode(self.q, self.case.k_cache, self.case.v_cache, self.bt, self.seq_lens,
+                          self.max_len, self.scale, self.window, 0, key=self.key,
+                          value=self.value, slot_mapping=self.slots, out=self.out,
+                          workspace=self.ws)
+
+    def attention_only(self):
+        self.pa.pa_decode(self.q, self.case.k_cache, self.case.v_cache, self.bt, self.seq_lens,
+                          self.max_len, self.scale, self.window, 0, out=self.out,
+                          workspace=self.ws)
+
+    # End-to-end: the step's inputs come from pinned host memory, the output goes back.
+    def host_buffers(self):
+        pin = lambda t: t.cpu().pin_memory()
+        self.h_in = [pin(x) for x in (self.q, self.key, self.value, self.slots, self.bt,
+                                      self.seq_lens)]
+        self.d_in = [torch.empty_like(x) for x in (self.q, self.key, self.value, self.slots,
+                                                   self.bt, self.seq_lens)]
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = sum(x.numel() * x.element_size() for x in self.h_in)
+        self.d2h = self.h_out.numel() * self.h_out.element_size()
+
+    def e2e_step(self):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        q, key, value, slots, bt, sl = self.d_in
+        self.pa.pa_decode(q, self.case.k_cache, self.case.v_cache, bt, sl, self.max_len,
+                          self.scale, self.window, 0, key=key, value=value, slot_mapping=slots,
+                          out=self.out, workspace=self.ws)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+class PrefillRunner:
+    """One step: fused store of the prompt tokens + varlen causal prefill."""
+
+    def __init__(self, case, device):
+        import paged_kv_attention_03_gb300 as pa
+
+        self.pa = pa
+        self.case = case
+        w = case.workload
+        t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=device)
+        self.cu = t(case.cu_seqlens_q)
+        self.seq_lens = t(case.seq_lens)
+        self.bt = t(case.block_table)
+        self.slots = t(case.slot_mapping)
+        self.out = torch.empty_like(case.q)
+        self.launches = 2
+        self.work = prefill_flops(case)
+
+    def step(self):
+        c = self.case
+        self.pa.pa_varlen_prefill(c.q, c.k_cache, c.v_cache, self.cu, self.seq_lens, self.bt,
+                                  c.max_query_len, c.max_seq_len, c.workload.final_scale,
+                                  c.workload.sliding_window, key=c.key, value=c.value,
+                                  slot_mapping=self.slots, out=self.out)
+
+    def attention_only(self):
+        c = self.case
+        self.pa.pa_varlen_prefill(c.q, c.k_cache, c.v_cache, self.cu, self.seq_lens, self.bt,
+                                  c.max_query_len, c.max_seq_len, c.workload.final_scale,
+                                  c.workload.sliding_window, out=self.out)
+
+
+def _time_steps(fn, steps, warmup, flush, stream):
+    """Per-step device time (ms) with CUDA events on `stream`, L2 flushed (untimed) before
+    each step."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+# ------------------------------------------------------------ CPU baseline ---
+
+def oracle_decode_time(case, seqs, budget_s=12.0):
+    """Time the fp64 oracle (store + attention) on the given decode sequences, repeating
+    the sample until about `budget_s` seconds of CPU work; returns (s per sample, threads)."""
+    import oracle
+    from paged_kv_attention_03_gb300.inputs import bf16_bits
+
+    w = case.workload
+    seqs = np.asarray(seqs)
+    cu = case.cu_seqlens_q
+    rows = cu[seqs]
+    q = bf16_bits(case.q)[rows]
+    key = bf16_bits(case.key)[rows]
+    value = bf16_bits(case.value)[rows]
+    kc = bf16_bits(case.k_cache)
+    vc = bf16_bits(case.v_cache)
+    slots = np.ascontiguousarray(case.slot_mapping[rows])
+    sub_cu = np.arange(len(seqs) + 1, dtype=np.int32)
+    bt = np.ascontiguousarray(case.block_table[seqs])
+    sl = np.ascontiguousarray(case.seq_lens[seqs])
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle.store_kvcache(key, value, kc, vc, slots, w.block_size)
+        oracle.paged_attention(q, kc, vc, sub_cu, sl, bt, w.num_heads, w.num_kv_heads,
+                               w.sliding_window, w.final_scale, threads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 50:
+            break
+    return statistics.median(times), threads, len(times)
+
+
+# -------------------------------------------------------------------- main ---
+
+def run_reference(args, rank, ws):
+    """The fp64 CPU oracle as the reference arm, on a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_attention_03_gb300.inputs import bf16_bits
+
+    wl = WORKLOADS[args.workload]
+    case = make_case(wl, seed=0, device="cpu")
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    order = np.argsort(case.seq_lens)
+    # Sequences per step: sized so warmup + steps fit in about two minutes.
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    probe = [int(order[len(order) // 2])]
+    t_probe, _, _ = oracle_decode_time(case, probe, budget_s=0.0)
+    n = max(1, min(case.num_seqs, int(per_step_budget / max(t_probe, 1e-6))))
+    rng = np.random.default_rng(0)
+    q_bits, kc, vc = bf16_bits(case.q), bf16_bits(case.k_cache), bf16_bits(case.v_cache)
+    key, value = bf16_bits(case.key), bf16_bits(case.value)
+    w = case.workload
+    times, work = [], []
+    for it in range(args.warmup + args.steps):
+        seqs = np.sort(rng.choice(case.num_seqs, size=n, replace=False))
+        rows = case.cu_seqlens_q[seqs]
+        t0 = time.perf_counter()
+        oracle.store_kvcache(key[rows], value[rows], kc, vc,
+                             np.ascontiguousarray(case.slot_mapping[rows]), w.block_size)
+        oracle.paged_attention(np.ascontiguousarray(q_bits[rows]), kc, vc,
+                               np.arange(n + 1, dtype=np.int32),
+                               np.ascontiguousarray(case.seq_lens[seqs]),
+                               np.ascontiguousarray(case.block_table[seqs]), w.num_heads,
+                               w.num_kv_heads, w.sliding_window, w.final_scale, threads)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            times.append(dt)
+            work.append(decode_kv_bytes(case, seqs))
+    total_t = sum(times)
+    value_gbs = sum(work) / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": "decode KV-read GB/s", "value": round(value_gbs, 4),
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {_describe(wl)}", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value_gbs, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{n} of {case.num_seqs} sequences per step (random), "
+                                   f"store + fp64 attention"},
+        "e2e": {"value": round(value_gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _describe(wl):
+    return (f"H={wl.num_heads} Hkv={wl.num_kv_heads} D={wl.head_dim} bs={wl.block_size} "
+            f"groups={wl.groups} window={wl.sliding_window}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="batched_decode",
+                    choices=["batched_decode", "long_decode", "tiny_decode", "mixed_window"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank, local, ws = _dist()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+        return
+
+    import paged_kv_attention_03_gb300 as pa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pa.build()
+    pa.load()
+    peaks = _peaks()
+    wl = WORKLOADS[args.workload]
+    # Weak scaling: every rank runs its own replica (own seed), no data-path collective.
+    case = make_case(wl, seed=rank, device=dev)
+    seqs = None
+    if args.workload == "mixed_window":
+        seqs = split_mixed(case)[1]
+    runner = DecodeRunner(case, dev, seqs)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(args.warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    step_ms = _time_steps(runner.step, args.steps, 0, flush, stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    # Attention call alone (split kernel + combine, no store): the roofline numerator.
+    attn_ms = _time_steps(runner.attention_only, max(20, args.steps // 4), 3, flush, stream)
+    clocks = sampler.stop() if sampler else None
+
+    total_ms = _max_over_ranks(sum(step_ms), ws, dev)
+    units = _sum_over_ranks(runner.work * args.steps, ws, dev)
+    value = units / (total_ms / 1e3) / 1e9
+    ms_per_step = total_ms / args.steps
+    attn_mean = statistics.mean(attn_ms)
+    achieved = runner.work / (attn_mean / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        runner.host_buffers()
+        e2e_ms = []
+        for _ in range(3):
+            flush.zero_()
+            runner.e2e_step()
+        torch.cuda.synchronize()
+        for _ in range(max(20, args.steps // 4)):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            runner.e2e_step()
+            torch.cuda.synchronize()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        e2e_t = _max_over_ranks(statistics.mean(e2e_ms), ws, dev)
+        e2e = {"value": round(_sum_over_ranks(runner.work, ws, dev) / (e2e_t / 1e3) / 1e9, 3),
+               "unit": "GB/s", "h2d_bytes_per_step": runner.h2d,
+               "d2h_bytes_per_step": runner.d2h, "ms_per_step": round(e2e_t, 4)}
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = _prefill_leg(pa, dev, rank, peaks, flush, stream, args)
+
+    cpu = None
+    if rank == 0 and ws >= 1 and not args.no_cpu_baseline and args.gpus == 1:
+        t_s, threads, reps = oracle_decode_time(case, runner.seqs)
+        cpu = {"value": round(runner.work / t_s / 1e9, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"the whole step ({len(runner.seqs)} sequences: store + fp64 "
+                         f"attention), median of {reps} runs"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "decode KV-read GB/s", "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {_describe(wl)}",
+                   "batch": len(runner.seqs), "kv_bytes_per_step": runner.work,
+                   "num_splits": runner.splits,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_split_kernel + combine)",
+                     "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"], "traffic": None,
+                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": runner.launches * args.steps,
+        "clocks": clocks,
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    print(json.dumps(line), flush=True)
+
+
+def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):
+    """TFLOP/s of the varlen causal prefill workload (store + prefill), or None if the
+    prefill entry point is not available in this build."""
+    case = make_case(WORKLOADS["varlen_prefill"], seed=100 + rank, device=dev)
+    runner = PrefillRunner(case, dev)
+    try:
+        runner.step()
+        torch.cuda.synchronize()
+    except pa.PAError as e:
+        return {"status": f"unavailable: {e}"}
+    steps = max(20, args.steps // 10)
+    ms = _time_steps(runner.step, steps, 3, flush, stream)
+    attn = _time_steps(runner.attention_only, steps, 3, flush, stream)
+    tf = runner.work / (statistics.mean(ms) / 1e3) / 1e12
+    ach = runner.work / (statistics.mean(attn) / 1e3) / 1e12
+    return {"metric": "varlen prefill TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(statistics.mean(ms), 4), "flops_per_step": runner.work,
+            "workload": "varlen_prefill: 16 prompts U[128,2048], 32/8 heads, D=128, bs=16",
+            "roofline": {"bound": "tensor", "kernel": "pa_varlen_prefill",
+                         "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                         "peak_source": peaks["source"]}}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * pa_gb300.h - C ABI of the GB300 (sm_103a) paged KV-cache attention library
+ * (libpa_gb300.so).
+ *
+ * Three operations, each on one GPU and asynchronous on the caller's stream:
+ *
+ *   pa_store_kvcache   write new K/V rows into the paged cache through slot_mapping
+ *   pa_decode          one query per sequence over its paged K/V (split-K + combine)
+ *   pa_varlen_prefill  packed variable-length causal / chunked / sliding-window prefill
+ *
+ * Common conventions
+ *   - Element type: every q / k / v / cache / out buffer is bf16, row-major as stated.
+ *   - Cache layout: k_cache and v_cache are the two halves of the
+ *     [2, num_blocks, block_size, num_kv_heads, head_dim] cache ("05 Attention
+ *     Backends", section 3, get_kv_cache_shape; "MinivLLM API docs - Attention",
+ *     paged_attention_decode), i.e. each is [num_blocks, block_size, num_kv_heads,
+ *     head_dim] with head_dim contiguous.  They may be two separate allocations.
+ *   - block_table: [num_seqs, max_num_blocks] int32, row-contiguous; entry (i, j) is
+ *     the physical block of logical block j of sequence i; entries past
+ *     ceil(seq_len / block_size) are never read and may be -1.
+ *   - seq_lens[i]: keys of sequence i in the cache, INCLUDING the tokens of this step
+ *     (seq_len = context_len + query_len, "05 Attention Backends", section 4).
+ *   - GQA: query head h uses kv head h / (num_heads / num_kv_heads)
+ *     ("vllm-npu 0.4.2, torch_sdpa.py", TorchSDPABackendImpl, num_queries_per_kv).
+ *   - Mask: the query_len queries of a sequence are its LAST query_len positions
+ *     (bottom-right causal alignment); with sliding_window = w > 0 a query at
+ *     position p sees keys p-w+1 .. p (w keys, its own included); w <= 0 means no
+ *     window ("transformers continuous_batching/input_ouputs.py",
+ *     build_attention_mask, and "vllm-npu 0.4.2, torch_sdpa.py",
+ *     _make_sliding_window_bias).
+ *   - scale is the final logit scale (normally 1/sqrt(head_dim)).
+ *   - Arithmetic: bf16 operands, fp32 accumulation, bf16 output (round to nearest).
+ *   - Ownership: the caller owns every buffer (inputs, outputs, the cache and any
+ *     workspace).  The library allocates no device memory on these calls and keeps
+ *     no pointer after a call returns.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; inputs must stay valid until it finishes.
+ *   - Errors: argument errors are found on the host before anything is launched and
+ *     return PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED; a failed launch returns
+ *     PA_ERR_CUDA.  Conditions only visible on the device (a slot or block index out
+ *     of range, seq_len larger than the declared maximum, query_len > seq_len) never
+ *     make a kernel touch memory outside its buffers: the offending row is skipped or
+ *     zero-filled and a bit is OR-ed into a per-device error word that
+ *     pa_read_device_error returns.  Nothing throws across this ABI.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes, misalignment */
+    PA_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, block_size, group size */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE_CHECK = 4 /* pa_read_device_error found device-side check bits set */
+} pa_status;
+
+/* Bits of the device error word (see pa_read_device_error). */
+#define PA_DEVERR_SLOT_RANGE 0x1u  /* store: slot >= num_blocks * block_size (row skipped) */
+#define PA_DEVERR_BLOCK_RANGE 0x2u /* block_table entry outside [0, num_blocks) (zero-filled) */
+#define PA_DEVERR_SEQ_RANGE 0x4u   /* seq_len > max_num_blocks*block_size or > max_seq_len */
+#define PA_DEVERR_QUERY_LEN 0x8u   /* prefill: query_len > seq_len, or > max_seqlen_q */
+#define PA_DEVERR_SEQLENS_K 0x10u  /* prefill: cu_seqlens_k differences disagree with seq_lens */
+
+/* Human-readable name of a status code (static storage). */
+const char *pa_status_string(pa_status status);
+
+/* Library version, e.g. "pa_gb300 0.1 sm_103a". */
+const char *pa_version(void);
+
+/*
+ * pa_store_kvcache - "MinivLLM API docs - Attention", section store_kvcache, and
+ * "05 Attention Backends", Q&A 2 (slot -> block, offset).
+ *
+ * For every token t in [0, num_tokens) with s = slot_mapping[t] >= 0:
+ *     k_cache[s / block_size][s % block_size][:][:] = key[t][:][:]
+ *     v_cache[s / block_size][s % block_size][:][:] = value[t][:][:]
+ * Negative slots (padding, -1 on the page) are skipped.  Bit-exact copy.
+ *
+ *   key, value    [num_tokens, num_kv_heads, head_dim] bf16, device, 16-byte aligned
+ *   k_cache/v_cache [num_blocks, block_size, num_kv_heads, head_dim] bf16, device,
+ *                 16-byte aligned
+ *   slot_mapping  [num_tokens] int32, device
+ * Requires num_kv_heads * head_dim to be a multiple of 8.  Slots >= num_blocks *
+ * block_size are skipped and flagged PA_DEVERR_SLOT_RANGE.  Two tokens mapped to the
+ * same slot in one call leave either one's row (undefined which).
+ */
+pa_status pa_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+                           const int32_t *slot_mapping, int64_t num_tokens,
+                           int64_t num_blocks, int block_size, int num_kv_heads,
+                           int head_dim, void *stream);
+
+/*
+ * Split-K planning for pa_decode.  The KV range of each (sequence, kv-head group)
+ * is cut into at most `num_splits` slices processed by separate CTAs and merged by
+ * a log-sum-exp combine.  pa_decode_num_splits returns the slice count pa_decode
+ * will use for these arguments (num_splits <= 0 asks for the automatic choice);
+ * pa_decode_workspace_size returns the workspace bytes pa_decode needs for them
+ * (0 when one slice suffices).  Both return 0 for invalid arguments.
+ */
+int pa_decode_num_splits(int batch, int num_heads, int num_kv_heads, int head_dim,
+                         int max_seq_len, int sliding_window, int num_splits);
+size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                int max_seq_len, int sliding_window, int num_splits);
+
+/*
+ * pa_decode - paged attention for one new query per sequence.  "MinivLLM API docs
+ * - Attention", section paged_attention_decode; "vllm-npu 0.4.2, xformers.py",
+ * XFormersImpl.forward (decode branch, PagedAttention.forward_decode); the split-KV
+ * merge follows "05 Attention Backends", section 7.1 (split-KV for long decode).
+ *
+ * For each sequence b (L = seq_lens[b]) and query head h:
+ *     out[b][h] = sum_j softmax_j(scale * q[b][h] . K_j) V_j
+ * over keys j in [max(0, L - w), L - 1] (all j < L without a window), K_j/V_j read
+ * from kv head h / (num_heads / num_kv_heads) through block_table.  L == 0 gives a
+ * zero row.
+ *
+ *   out           [batch, num_heads, head_dim] bf16, device (written)
+ *   q             [batch, num_heads, head_dim] bf16, device, 16-byte aligned
+ *   key, value, slot_mapping   optional (all NULL or all set): [batch, num_kv_heads,
+ *                 head_dim] bf16 and [batch] int32.  When set, the call first stores
+ *                 them into the cache exactly as pa_store_kvcache (same stream), so
+ *                 the new token is visible to the attention that follows.
+ *   k_cache, v_cache  the paged cache (written only by that optional store)
+ *   block_table   [batch, max_num_blocks] int32, device
+ *   seq_lens      [batch] int32, device
+ *   max_seq_len   host-side upper bound of seq_lens (sizes the split-K grid); a larger
+ *                 seq_len is flagged PA_DEVERR_SEQ_RANGE and truncated
+ *   num_splits    <= 0: automatic; otherwise an upper bound on the slice count
+ *   workspace     device scratch of at least pa_decode_workspace_size(...) bytes,
+ *                 256-byte aligned (may be NULL when that size is 0); its contents
+ *                 on entry do not matter
+ * Supported: head_dim in {64, 128}; block_size a power of two in [1, 1024];
+ * num_heads / num_kv_heads in [1, 64].
+ */
+pa_status pa_decode(void *out, const void *q, const void *key, const void *value,
+                    const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                    const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
+                    int batch, int max_seq_len, int64_t num_blocks, int block_size,
+                    int num_heads, int num_kv_heads, int head_dim, int sliding_window,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
+ * pa_varlen_prefill - packed variable-length causal / chunked prefill over the
+ * paged cache.  "MinivLLM API docs - Attention", section flash_attention_prefill
+ * (varlen packing by cu_seqlens, causal, GQA); "vllm-npu 0.4.2, xformers.py",
+ * XFormersImpl.forward (forward_prefix with a cached context, sliding window);
+ * "05 Attention Backends", section 5 (flash_attn_varlen_func with cu_seqlens_q,
+ * seqused_k, block_table); mask as build_attention_mask.
+ *
+ * Sequence i owns query rows [cu_seqlens_q[i], cu_seqlens_q[i+1]) of q and out
+ * (sq_i rows) and sk_i keys in the cache (sk_i = seq_lens[i], or
+ * cu_seqlens_k[i+1] - cu_seqlens_k[i] when seq_lens is NULL); sq_i <= sk_i.  Row r
+ * is the query at absolute position p = sk_i - sq_i + r and attends keys
+ * [max(0, p - w + 1), p] (all keys <= p without a window).  sq_i == 1 rows are
+ * legal, so a mixed prefill + decode batch may be passed as one call.
+ *
+ *   out           [total_q, num_heads, head_dim] bf16, device (written)
+ *   q             [total_q, num_heads, head_dim] bf16, device, 16-byte aligned
+ *   key, value, slot_mapping   optional (all NULL or all set): [total_q, num_kv_heads,
+ *                 head_dim] bf16 and [total_q] int32; stored first, as pa_store_kvcache
+ *   cu_seqlens_q  [num_seqs + 1] int32, device, non-decreasing, cu_seqlens_q[0] == 0,
+ *                 cu_seqlens_q[num_seqs] == total_q
+ *   cu_seqlens_k  [num_seqs + 1] int32 or NULL; when both it and seq_lens are given,
+ *                 seq_lens is used and a disagreement is flagged PA_DEVERR_SEQLENS_K
+ *   seq_lens      [num_seqs] int32 or NULL (not both NULL)
+ *   block_table   [num_seqs, max_num_blocks] int32, device
+ *   max_seqlen_q  host-side upper bound of sq_i (sizes the grid); larger is flagged
+ *   max_seqlen_k  host-side upper bound of sk_i; larger is flagged
+ * Supported: head_dim in {64, 128}; block_size a power of two in [16, 256];
+ * num_heads / num_kv_heads in [1, 128].
+ */
+pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
+                            const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *seq_lens, const int32_t *block_table,
+                            int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
+                            int max_seqlen_k, int64_t num_blocks, int block_size,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int sliding_window, float scale, void *stream);
+
+/*
+ * pa_read_device_error - synchronise `stream`, then return in *flags the device
+ * error word of the current device (PA_DEVERR_* bits OR-ed by every launch since it
+ * was last cleared) and clear it when `clear` is non-zero.  Returns PA_OK when no
+ * bit is set, PA_ERR_DEVICE_CHECK when some bit is set, PA_ERR_CUDA on a CUDA
+ * failure.  flags may be NULL.
+ */
+pa_status pa_read_device_error(void *stream, uint32_t *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

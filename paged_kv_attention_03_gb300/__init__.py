@@ -1,0 +1,33 @@
+"""GB300-native attention over a paged, block-structured KV cache.
+
+The product is ``libpa_gb300.so`` (C ABI in ``include/pa_gb300.h``), built from
+``csrc/`` for sm_103a.  This package is its thin Python binding (same names as the
+C entry points), the build step, and the seeded input generator used by tests and
+the benchmark.  Importing the package does not load the library; the first call
+does, and raises if it is missing.
+"""
+from ._lib import (  # noqa: F401
+    DEVERR_BLOCK_RANGE,
+    DEVERR_QUERY_LEN,
+    DEVERR_SEQ_RANGE,
+    DEVERR_SEQLENS_K,
+    DEVERR_SLOT_RANGE,
+    EXPORTED,
+    PA_ERR_CUDA,
+    PA_ERR_DEVICE_CHECK,
+    PA_ERR_INVALID_ARG,
+    PA_ERR_UNSUPPORTED,
+    PA_OK,
+    PAError,
+    library_path,
+    load,
+    pa_decode,
+    pa_decode_num_splits,
+    pa_decode_workspace_size,
+    pa_read_device_error,
+    pa_store_kvcache,
+    pa_varlen_prefill,
+    status_string,
+    version,
+)
+from .build import build  # noqa: F401

@@ -1,0 +1,227 @@
+"""ctypes binding of libpa_gb300.so (the C ABI declared in include/pa_gb300.h).
+
+Argument marshalling only: tensors become raw device pointers, the current CUDA
+stream becomes a cudaStream_t, and every computation runs in the library's kernels.
+There is no CPU path: if the library is missing or a call fails, an exception says
+so.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE_CHECK = range(5)
+DEVERR_SLOT_RANGE = 0x1
+DEVERR_BLOCK_RANGE = 0x2
+DEVERR_SEQ_RANGE = 0x4
+DEVERR_QUERY_LEN = 0x8
+DEVERR_SEQLENS_K = 0x10
+
+EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
+            "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
+            "pa_read_device_error")
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load the shared library (building it first if it is missing and allowed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libpa_gb300.so is not built ({path}); run build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                 ctypes.c_float, ctypes.c_size_t)
+        lib.pa_status_string.argtypes = [ctypes.c_int]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_version.argtypes = []
+        lib.pa_version.restype = ctypes.c_char_p
+        lib.pa_store_kvcache.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, vp]
+        lib.pa_store_kvcache.restype = ctypes.c_int
+        lib.pa_decode_num_splits.argtypes = [i32] * 7
+        lib.pa_decode_num_splits.restype = ctypes.c_int
+        lib.pa_decode_workspace_size.argtypes = [i32] * 7
+        lib.pa_decode_workspace_size.restype = sz
+        lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64, i32,
+                                  i32, i32, i32, i32, f32, i32, vp, sz, vp]
+        lib.pa_decode.restype = ctypes.c_int
+        lib.pa_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                          i32, i32, i32, i64, i32, i32, i32, i32, i32, f32, vp]
+        lib.pa_varlen_prefill.restype = ctypes.c_int
+        lib.pa_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        lib.pa_read_device_error.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().pa_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still describe the code
+        return str(status)
+
+
+def version() -> str:
+    return load().pa_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PAError(status, what)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str, device: torch.device | None = None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def pa_store_kvcache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, slot_mapping: torch.Tensor) -> None:
+    """Scatter key/value [T, Hkv, D] into k_cache/v_cache [NB, bs, Hkv, D] by slot_mapping [T]."""
+    lib = load()
+    dev = k_cache.device
+    for t, n in ((key, "key"), (value, "value"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    nb, bs, hkv, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or key.shape != value.shape or key.shape[1:] != (hkv, d):
+        raise ValueError("store_kvcache: inconsistent shapes")
+    if slot_mapping.shape[0] != key.shape[0]:
+        raise ValueError("store_kvcache: slot_mapping length != number of tokens")
+    st = lib.pa_store_kvcache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d, _stream(dev))
+    _check(st, "pa_store_kvcache")
+
+
+def pa_decode_num_splits(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                         max_seq_len: int, sliding_window: int = 0, num_splits: int = 0) -> int:
+    return int(load().pa_decode_num_splits(batch, num_heads, num_kv_heads, head_dim,
+                                           max_seq_len, sliding_window, num_splits))
+
+
+def pa_decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                             max_seq_len: int, sliding_window: int = 0,
+                             num_splits: int = 0) -> int:
+    return int(load().pa_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim,
+                                               max_seq_len, sliding_window, num_splits))
+
+
+def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+              scale: float, sliding_window: int = 0, num_splits: int = 0,
+              key: torch.Tensor | None = None, value: torch.Tensor | None = None,
+              slot_mapping: torch.Tensor | None = None, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Paged decode: q [B, H, D] -> out [B, H, D]; optional store of key/value first."""
+    lib = load()
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    batch, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
+        raise ValueError("pa_decode: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
+                                    sliding_window, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need else 0
+    st = lib.pa_decode(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                       _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                       _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                       head_dim, int(sliding_window), float(scale), int(num_splits), ws_ptr,
+                       ws_bytes, _stream(dev))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor | None,
+                      block_table: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                      scale: float, sliding_window: int = 0,
+                      cu_seqlens_k: torch.Tensor | None = None,
+                      key: torch.Tensor | None = None, value: torch.Tensor | None = None,
+                      slot_mapping: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """Packed varlen causal/chunked prefill: q [Tq, H, D] -> out [Tq, H, D]."""
+    lib = load()
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    if seq_lens is not None:
+        _need(seq_lens, torch.int32, "seq_lens", dev)
+    if cu_seqlens_k is not None:
+        _need(cu_seqlens_k, torch.int32, "cu_seqlens_k", dev)
+    total_q, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    num_seqs = cu_seqlens_q.shape[0] - 1
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("pa_varlen_prefill: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.pa_varlen_prefill(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), _ptr(seq_lens), _ptr(block_table),
+                               block_table.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                               int(max_seqlen_k), nb, bs, num_heads, hkv, head_dim,
+                               int(sliding_window), float(scale), _stream(dev))
+    _check(st, "pa_varlen_prefill")
+    return out
+
+
+def pa_read_device_error(clear: bool = True, device: torch.device | None = None) -> int:
+    """Synchronise the current stream and return (and optionally clear) the device error word."""
+    lib = load()
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    flags = ctypes.c_uint32(0)
+    st = lib.pa_read_device_error(_stream(dev), ctypes.byref(flags), 1 if clear else 0)
+    if st not in (PA_OK, PA_ERR_DEVICE_CHECK):
+        raise PAError(st, "pa_read_device_error")
+    return int(flags.value)

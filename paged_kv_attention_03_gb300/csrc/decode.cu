@@ -1,0 +1,507 @@
+// decode.cu - split-K flash-decoding over the paged KV cache, plus the LSE combine.
+//
+// What it computes ("MinivLLM API docs - Attention", section paged_attention_decode;
+// "vllm-npu 0.4.2, xformers.py", decode branch): for sequence b with L = seq_lens[b]
+// keys and query head h, out[b][h] = softmax(scale * q K^T) V over keys
+// [max(0, L - w), L) (w = sliding window, or all keys), K/V of kv head
+// h / (num_heads / num_kv_heads), read through block_table.
+//
+// GB300 design (the page's Triton kernel runs one program per (sequence, query
+// head) and streams the whole context once per query head):
+//  * One CTA per (sequence, kv head, 16-head tile, split).  All query heads that
+//    share a kv head sit in the same CTA, so each K/V byte is read from HBM once per
+//    kv head, not once per query head.
+//  * The split's key range is cut into 16-key units; warp w takes units w, w + NW,
+//    ... and streams them through its own NSTAGES-deep cp.async ring (16-byte
+//    copies, XOR-swizzled so ldmatrix is bank-conflict free).  Block-table lookups
+//    are per key row, so any power-of-two block_size works.
+//  * S = Q K^T and O += P V run on the bf16 warp MMA (m16n8k16, fp32 accumulate)
+//    with the query heads of the group as the M = 16 rows.  Decode is HBM bound; the
+//    MMA only keeps the issue slots free (a CUDA-core dot product would need about
+//    one FFMA per loaded element per query head).
+//  * Online softmax in the base-2 domain with 2-step warp shuffles per row; the
+//    warps of a CTA merge their (m, l, O) through shared memory; a split writes
+//    either the final bf16 row (single split) or a normalised fp32 partial plus
+//    (m, l) to the workspace for decode_combine_kernel.
+#include <math.h>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+struct DecodeKernelParams {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    const int32_t *block_table;
+    int max_num_blocks;
+    const int32_t *seq_lens;
+    int64_t seq_cap;  // min(max_num_blocks * block_size, max_seq_len)
+    int64_t num_blocks;
+    int log2_bs;
+    int num_heads;
+    int num_kv_heads;
+    int group;
+    int head_tiles;
+    int window;
+    float scale_log2;  // scale * log2(e)
+    int chunk;
+    int num_splits;
+    float *ws_o;   // [batch, num_heads, num_splits, D] normalised partial outputs
+    float *ws_ml;  // [batch, num_heads, num_splits, 2] (running max in log2 units, sum)
+    unsigned *err;
+};
+
+// Key range of one sequence: keys [start, L); splits tile [base, L) in `chunk`s.
+struct SeqRange {
+    int L;
+    int start;
+    int base;
+};
+
+__device__ __forceinline__ SeqRange decode_range(int raw_len, int64_t cap, int window,
+                                                 unsigned *err, bool report) {
+    SeqRange r;
+    int L = raw_len;
+    if (L < 0 || static_cast<int64_t>(L) > cap) {
+        if (report) flag_error(err, kErrSeqRange);
+        L = L < 0 ? 0 : static_cast<int>(cap);
+    }
+    r.L = L;
+    r.start = window > 0 ? max(0, L - window) : 0;
+    r.base = r.start & ~15;
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+template <int D, int NWARPS, int NSTAGES>
+__global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const DecodeKernelParams p) {
+    constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
+    constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
+    constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
+    constexpr int CPR = D / 8;                // 16-byte chunks per row
+    constexpr int ROWS_PER_PASS = 32 / CPR;
+    constexpr int PASSES = 16 / ROWS_PER_PASS;
+    constexpr int KSTEPS = D / 16;
+    constexpr int DTILES = D / 8;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int split = blockIdx.x;
+    const int b = blockIdx.z;
+    const int kvh = blockIdx.y / p.head_tiles;
+    const int ht = blockIdx.y - kvh * p.head_tiles;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const bool report = split == 0 && blockIdx.y == 0 && threadIdx.x == 0;
+    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window, p.err, report);
+    const int lo = max(sr.start, sr.base + split * p.chunk);
+    const int hi = min(sr.L, sr.base + (split + 1) * p.chunk);
+    const int h0 = kvh * p.group + ht * 16;
+    const int rows_valid = min(16, p.group - ht * 16);
+
+    if (lo >= hi) {
+        // Empty split.  A sequence with no keys at all gets a zero row; with several
+        // splits the combine kernel writes it.
+        if (p.num_splits == 1 && sr.L == 0) {
+            for (int i = threadIdx.x; i < rows_valid * D; i += NWARPS * 32)
+                p.out[(static_cast<int64_t>(b) * p.num_heads + h0) * D + i] =
+                    __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+
+    // Q fragments (A operand, 16 rows = query heads of this tile, zero padded).
+    uint32_t qa[KSTEPS][4];
+    {
+        const __nv_bfloat16 *qb = p.q + (static_cast<int64_t>(b) * p.num_heads + h0) * D;
+        const int r0 = lane >> 2;
+        const int c0 = (lane & 3) * 2;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            qa[ks][0] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0) : 0u;
+            qa[ks][1] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0) : 0u;
+            qa[ks][2] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0 + 8) : 0u;
+            qa[ks][3] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0 + 8) : 0u;
+        }
+    }
+
+    const int u_first = lo >> 4;
+    const int u_last = (hi - 1) >> 4;
+    const int32_t *bt_row = p.block_table + static_cast<int64_t>(b) * p.max_num_blocks;
+    const int bs_mask = (1 << p.log2_bs) - 1;
+    uint8_t *my_stages = smem + warp * NSTAGES * STAGE_BYTES;
+    const uint32_t stage_base = smem_u32(my_stages);
+    const uint64_t policy = l2_policy_evict_first();
+
+    auto issue = [&](int u, int st) {
+        const uint32_t sb = stage_base + st * STAGE_BYTES;
+        const int c = lane % CPR;
+        const int rsub = lane / CPR;
+#pragma unroll
+        for (int i = 0; i < PASSES; ++i) {
+            const int r = i * ROWS_PER_PASS + rsub;
+            const int j = u * 16 + r;
+            const __nv_bfloat16 *ksrc = p.k_cache;
+            const __nv_bfloat16 *vsrc = p.v_cache;
+            uint32_t nbytes = 0;
+            if (j >= lo && j < hi) {
+                const int blk = __ldg(bt_row + (j >> p.log2_bs));
+                if (blk < 0 || blk >= p.num_blocks) {
+                    flag_error(p.err, kErrBlockRange);
+                } else {
+                    const int64_t off =
+                        (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
+                             p.num_kv_heads + kvh) * D + c * 8;
+                    ksrc = p.k_cache + off;
+                    vsrc = p.v_cache + off;
+                    nbytes = 16;
+                }
+            }
+            const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
+            cp_async_16_policy(sb + so, ksrc, nbytes, policy);
+            cp_async_16_policy(sb + TILE_BYTES + so, vsrc, nbytes, policy);
+        }
+    };
+
+    float o[DTILES][4];
+#pragma unroll
+    for (int i = 0; i < DTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+
+    const int my_first = u_first + warp;
+    // Prologue: NSTAGES - 1 units in flight.
+#pragma unroll
+    for (int st = 0; st < NSTAGES - 1; ++st) {
+        const int u = my_first + st * NWARPS;
+        if (u <= u_last) issue(u, st);
+        cp_async_commit();
+    }
+
+    int it = 0;
+    for (int u = my_first; u <= u_last; u += NWARPS, ++it) {
+        {
+            const int un = u + (NSTAGES - 1) * NWARPS;
+            if (un <= u_last) issue(un, (it + NSTAGES - 1) % NSTAGES);
+            cp_async_commit();
+        }
+        cp_async_wait<NSTAGES - 1>();
+        __syncwarp();
+
+        const uint32_t kb = stage_base + (it % NSTAGES) * STAGE_BYTES;
+        const uint32_t vb = kb + TILE_BYTES;
+
+        // S = Q K^T for 16 keys: two n-tiles of 8 keys.
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int r = ((lane >> 4) << 3) + (lane & 7);
+            const int chi = (lane >> 3) & 1;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint32_t kf[4];
+                const int ch = 2 * ks + chi;
+                ldmatrix_x4(kf, kb + r * ROWB + ((ch ^ (r & 7)) << 4));
+                mma_bf16_16816(s[0], qa[ks], kf[0], kf[1]);
+                mma_bf16_16816(s[1], qa[ks], kf[2], kf[3]);
+            }
+        }
+
+        // Mask, online softmax (rows lane/4 and lane/4 + 8 of the head tile).
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = u * 16 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                const float v = (j >= lo && j < hi) ? s[nt][e] * p.scale_log2 : -INFINITY;
+                s[nt][e] = v;
+                mx[e >> 1] = fmaxf(mx[e >> 1], v);
+            }
+        }
+        float corr[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+            const float m_new = fmaxf(m_run[i], mx[i]);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            corr[i] = exp2f(m_run[i] - m_use);
+            m_run[i] = m_new;
+            mx[i] = m_use;
+        }
+        float rowsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float pv = exp2f(s[nt][e] - mx[e >> 1]);
+                s[nt][e] = pv;
+                rowsum[e >> 1] += pv;
+            }
+        }
+        l_run[0] = l_run[0] * corr[0] + rowsum[0];
+        l_run[1] = l_run[1] * corr[1] + rowsum[1];
+#pragma unroll
+        for (int dt = 0; dt < DTILES; ++dt) {
+            o[dt][0] *= corr[0];
+            o[dt][1] *= corr[0];
+            o[dt][2] *= corr[1];
+            o[dt][3] *= corr[1];
+        }
+
+        // O += P V (P as the A operand straight from the S accumulators).
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+        {
+            const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
+            const int chi = lane >> 4;
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                uint32_t vf[4];
+                const int ch = 2 * dp + chi;
+                ldmatrix_x4_trans(vf, vb + r * ROWB + ((ch ^ (r & 7)) << 4));
+                mma_bf16_16816(o[2 * dp], pa, vf[0], vf[1]);
+                mma_bf16_16816(o[2 * dp + 1], pa, vf[2], vf[3]);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+        l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
+    }
+
+    // Merge the warps of the CTA through shared memory (the stage ring is free now).
+    __syncthreads();
+    constexpr int OSTRIDE = D + 4;
+    float *m_s = reinterpret_cast<float *>(smem);
+    float *l_s = m_s + NWARPS * 16;
+    float *o_s = l_s + NWARPS * 16;
+    {
+        const int r0 = lane >> 2;
+        if ((lane & 3) == 0) {
+            m_s[warp * 16 + r0] = m_run[0];
+            m_s[warp * 16 + r0 + 8] = m_run[1];
+            l_s[warp * 16 + r0] = l_run[0];
+            l_s[warp * 16 + r0 + 8] = l_run[1];
+        }
+        float *ow = o_s + warp * 16 * OSTRIDE;
+#pragma unroll
+        for (int dt = 0; dt < DTILES; ++dt) {
+            const int d = dt * 8 + (lane & 3) * 2;
+            *reinterpret_cast<float2 *>(ow + r0 * OSTRIDE + d) = make_float2(o[dt][0], o[dt][1]);
+            *reinterpret_cast<float2 *>(ow + (r0 + 8) * OSTRIDE + d) =
+                make_float2(o[dt][2], o[dt][3]);
+        }
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < rows_valid * D; idx += NWARPS * 32) {
+        const int row = idx / D;
+        const int d = idx - row * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, m_s[w * 16 + row]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+            const float mw = m_s[w * 16 + row];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            L += f * l_s[w * 16 + row];
+            acc += f * o_s[(w * 16 + row) * OSTRIDE + d];
+        }
+        const float res = acc / L;
+        const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h0 + row;
+        if (p.num_splits == 1) {
+            p.out[bh * D + d] = __float2bfloat16_rn(res);
+        } else {
+            p.ws_o[(bh * p.num_splits + split) * D + d] = res;
+            if (d == 0) {
+                p.ws_ml[(bh * p.num_splits + split) * 2] = M;
+                p.ws_ml[(bh * p.num_splits + split) * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// Log-sum-exp merge of the splits of one (sequence, head) per warp:
+//   M = max_s m_s,  w_s = l_s * 2^(m_s - M),  out = sum_s w_s O_s / sum_s w_s
+// where O_s are the normalised split outputs.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelParams p,
+                                                             int batch) {
+    constexpr int PER_LANE = D / 32;
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int b = gw / p.num_heads;
+    const int h = gw - b * p.num_heads;
+    if (b >= batch) return;
+    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window, p.err, false);
+    const int nsplit = sr.L > 0 ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
+    const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h;
+    __nv_bfloat16 *dst = p.out + bh * D + lane * PER_LANE;
+    if (nsplit == 0) {
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) dst[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const float *ml = p.ws_ml + bh * p.num_splits * 2;
+    const float *os = p.ws_o + bh * p.num_splits * D + lane * PER_LANE;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+    float wsum = 0.f;
+    float acc[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+        const float w = ml[2 * s + 1] * exp2f(ml[2 * s] - M);
+        wsum += w;
+        const float *src = os + static_cast<int64_t>(s) * D;
+        if constexpr (PER_LANE == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+            acc[2] += w * v.z;
+            acc[3] += w * v.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
+        }
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; i += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(dst + i) =
+            __floats2bfloat162_rn(acc[i] * inv, acc[i + 1] * inv);
+}
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 4;
+
+template <int D>
+constexpr int decode_smem_bytes() {
+    return kDecodeWarps * kDecodeStages * 2 * 16 * D * 2;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan, int batch,
+                            cudaStream_t stream) {
+    constexpr int smem = decode_smem_bytes<D>();
+    static_assert(smem >= (kDecodeWarps * 16 * 2 + kDecodeWarps * 16 * (D + 4)) * 4,
+                  "merge area must fit in the stage ring");
+    auto kern = decode_split_kernel<D, kDecodeWarps, kDecodeStages>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
+    kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || plan.num_splits == 1) return e;
+    const int warps = batch * kp.num_heads;
+    decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(kp, batch);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seq_len,
+                 int sliding_window, int num_splits_request, DecodePlan *plan) {
+    if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        head_dim <= 0 || max_seq_len < 0)
+        return false;
+    DecodePlan p;
+    p.group = num_heads / num_kv_heads;
+    p.head_tiles = (p.group + 15) / 16;
+    int64_t span = max_seq_len;
+    if (sliding_window > 0 && static_cast<int64_t>(sliding_window) + 15 < span)
+        span = static_cast<int64_t>(sliding_window) + 15;
+    p.span = static_cast<int>(span);
+    int splits;
+    if (span <= 0 || batch == 0) {
+        splits = 1;
+    } else if (num_splits_request > 0) {
+        splits = num_splits_request;
+    } else {
+        // Enough CTAs for ~16 per SM over the run (load balance across ragged
+        // lengths), but no split shorter than 256 keys (4 units per warp).
+        const int64_t units = static_cast<int64_t>(batch) * num_kv_heads * p.head_tiles;
+        const int64_t target = 16LL * 152;
+        int64_t s = (target + units - 1) / units;
+        const int64_t by_len = (span + 255) / 256;
+        if (s > by_len) s = by_len;
+        splits = static_cast<int>(s);
+    }
+    if (splits < 1) splits = 1;
+    if (splits > 1024) splits = 1024;
+    const int64_t span_pos = span > 0 ? span : 1;
+    int64_t chunk = (span_pos + splits - 1) / splits;
+    chunk = (chunk + 15) / 16 * 16;
+    p.chunk = static_cast<int>(chunk);
+    p.num_splits = static_cast<int>((span_pos + chunk - 1) / chunk);
+    *plan = p;
+    return true;
+}
+
+size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p) {
+    if (p.num_splits <= 1) return 0;
+    const size_t rows = static_cast<size_t>(batch) * num_heads * p.num_splits;
+    const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
+    return o_bytes + rows * 2 * sizeof(float);
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
+    if (a.batch == 0) return cudaSuccess;
+    DecodeKernelParams kp;
+    kp.out = static_cast<__nv_bfloat16 *>(a.out);
+    kp.q = static_cast<const __nv_bfloat16 *>(a.q);
+    kp.k_cache = static_cast<const __nv_bfloat16 *>(a.k_cache);
+    kp.v_cache = static_cast<const __nv_bfloat16 *>(a.v_cache);
+    kp.block_table = a.block_table;
+    kp.max_num_blocks = a.max_num_blocks;
+    kp.seq_lens = a.seq_lens;
+    int log2_bs = 0;
+    while ((1 << log2_bs) < a.block_size) ++log2_bs;
+    kp.log2_bs = log2_bs;
+    const int64_t table_cap = static_cast<int64_t>(a.max_num_blocks) << log2_bs;
+    kp.seq_cap = table_cap < a.max_seq_len ? table_cap : a.max_seq_len;
+    kp.num_blocks = a.num_blocks;
+    kp.num_heads = a.num_heads;
+    kp.num_kv_heads = a.num_kv_heads;
+    kp.group = plan.group;
+    kp.head_tiles = plan.head_tiles;
+    kp.window = a.sliding_window;
+    kp.scale_log2 = a.scale * kLog2e;
+    kp.chunk = plan.chunk;
+    kp.num_splits = plan.num_splits;
+    if (plan.num_splits > 1) {
+        const size_t rows = static_cast<size_t>(a.batch) * a.num_heads * plan.num_splits;
+        const size_t o_bytes = (rows * a.head_dim * sizeof(float) + 255) / 256 * 256;
+        kp.ws_o = static_cast<float *>(a.workspace);
+        kp.ws_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + o_bytes);
+    } else {
+        kp.ws_o = nullptr;
+        kp.ws_ml = nullptr;
+    }
+    kp.err = a.err;
+    switch (a.head_dim) {
+        case 64: return launch_decode_d<64>(kp, plan, a.batch, stream);
+        case 128: return launch_decode_d<128>(kp, plan, a.batch, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,258 @@
+// pa_api.cu - the extern "C" boundary of libpa_gb300.so (declared in pa_gb300.h).
+//
+// Host-side argument validation, the per-device error word, and dispatch to the
+// launchers.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/pa_gb300.h"
+#include "pa_internal.h"
+
+namespace {
+
+// One error word per device: kernels OR PA_DEVERR_* bits into it.
+__device__ unsigned int g_pa_device_error;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned *> g_err_ptr[kMaxDevices];
+std::mutex g_err_mutex;
+
+// Device address of this device's error word (looked up once per device).
+unsigned *device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned *p = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    p = g_err_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_pa_device_error) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned *>(addr);
+        g_err_ptr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+bool supported_head_dim(int d) { return d == 64 || d == 128; }
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Store-argument checks shared by the three entry points.
+pa_status check_store(const void *key, const void *value, const void *k_cache,
+                      const void *v_cache, const int32_t *slot_mapping, int64_t num_tokens,
+                      int64_t num_blocks, int block_size, int num_kv_heads, int head_dim) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if ((static_cast<int64_t>(num_kv_heads) * head_dim) % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa_status run_store(const void *key, const void *value, void *k_cache, void *v_cache,
+                    const int32_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                    int block_size, int num_kv_heads, int head_dim, cudaStream_t stream) {
+    pa::StoreArgs a;
+    a.key = key;
+    a.value = value;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slot_mapping = slot_mapping;
+    a.num_tokens = num_tokens;
+    a.num_slots = num_blocks * block_size;
+    a.row_elems = num_kv_heads * head_dim;
+    a.err = device_error_word();
+    return from_cuda(pa::launch_store_kvcache(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+const char *pa_version(void) { return "pa_gb300 0.1 sm_103a"; }
+
+pa_status pa_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+                           const int32_t *slot_mapping, int64_t num_tokens,
+                           int64_t num_blocks, int block_size, int num_kv_heads,
+                           int head_dim, void *stream) {
+    const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                     num_blocks, block_size, num_kv_heads, head_dim);
+    if (st != PA_OK || num_tokens == 0) return st;
+    return run_store(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                     block_size, num_kv_heads, head_dim, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_num_splits(int batch, int num_heads, int num_kv_heads, int head_dim,
+                         int max_seq_len, int sliding_window, int num_splits) {
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         num_splits, &plan))
+        return 0;
+    return plan.num_splits;
+}
+
+size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                int max_seq_len, int sliding_window, int num_splits) {
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         num_splits, &plan))
+        return 0;
+    return pa::decode_workspace_bytes(batch, num_heads, head_dim, plan);
+}
+
+pa_status pa_decode(void *out, const void *q, const void *key, const void *value,
+                    const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                    const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
+                    int batch, int max_seq_len, int64_t num_blocks, int block_size,
+                    int num_heads, int num_kv_heads, int head_dim, int sliding_window,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    if (batch < 0 || max_seq_len < 0 || num_blocks < 0 || max_num_blocks < 0 ||
+        num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size > 1024) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
+    const bool has_new = key || value || slot_mapping;
+    if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    if (max_seq_len > 0 && max_num_blocks == 0) return PA_ERR_INVALID_ARG;
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         num_splits, &plan))
+        return PA_ERR_INVALID_ARG;
+    const size_t need = pa::decode_workspace_bytes(batch, num_heads, head_dim, plan);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (has_new) {
+        const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, batch,
+                                         num_blocks, block_size, num_kv_heads, head_dim);
+        if (st != PA_OK) return st;
+        const pa_status rs = run_store(key, value, k_cache, v_cache, slot_mapping, batch,
+                                       num_blocks, block_size, num_kv_heads, head_dim, s);
+        if (rs != PA_OK) return rs;
+    }
+    pa::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.max_num_blocks = max_num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.max_seq_len = max_seq_len;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.sliding_window = sliding_window;
+    a.scale = scale;
+    a.workspace = workspace;
+    a.err = device_error_word();
+    return from_cuda(pa::launch_decode(a, plan, s));
+}
+
+pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
+                            const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *seq_lens, const int32_t *block_table,
+                            int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
+                            int max_seqlen_k, int64_t num_blocks, int block_size,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int sliding_window, float scale, void *stream) {
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+        num_blocks < 0 || max_num_blocks < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (max_seqlen_q > max_seqlen_k) return PA_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 128) return PA_ERR_UNSUPPORTED;
+    const bool has_new = key || value || slot_mapping;
+    if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !cu_seqlens_q) return PA_ERR_INVALID_ARG;
+    if (!seq_lens && !cu_seqlens_k) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    if (max_seqlen_k > 0 && max_num_blocks == 0) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (has_new) {
+        const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, total_q,
+                                         num_blocks, block_size, num_kv_heads, head_dim);
+        if (st != PA_OK) return st;
+        const pa_status rs = run_store(key, value, k_cache, v_cache, slot_mapping, total_q,
+                                       num_blocks, block_size, num_kv_heads, head_dim, s);
+        if (rs != PA_OK) return rs;
+    }
+    pa::PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.cu_seqlens_k = cu_seqlens_k;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.max_num_blocks = max_num_blocks;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.sliding_window = sliding_window;
+    a.scale = scale;
+    a.err = device_error_word();
+    return from_cuda(pa::launch_prefill(a, s));
+}
+
+pa_status pa_read_device_error(void *stream, uint32_t *flags, int clear) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    unsigned *word = device_error_word();
+    if (word == nullptr) return PA_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaMemcpy(&host, word, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (clear && host != 0) {
+        if (cudaMemset(word, 0, sizeof host) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (flags) *flags = host;
+    return host == 0 ? PA_OK : PA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

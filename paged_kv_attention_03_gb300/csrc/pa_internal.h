@@ -1,0 +1,86 @@
+// pa_internal.h - launcher interface between the C ABI (pa_api.cu) and the kernels.
+// Arguments reaching these launchers have already been validated on the host.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// ------------------------------------------------------------------ store ---
+struct StoreArgs {
+    const void *key;
+    const void *value;
+    void *k_cache;
+    void *v_cache;
+    const int32_t *slot_mapping;
+    int64_t num_tokens;
+    int64_t num_slots;  // num_blocks * block_size
+    int row_elems;      // num_kv_heads * head_dim (multiple of 8)
+    unsigned *err;
+};
+cudaError_t launch_store_kvcache(const StoreArgs &a, cudaStream_t stream);
+
+// ----------------------------------------------------------------- decode ---
+struct DecodePlan {
+    int group;        // query heads per kv head
+    int head_tiles;   // ceil(group / 16): 16-row MMA tiles per kv head
+    int span;         // longest key range one sequence can need (tokens)
+    int chunk;        // tokens per split (multiple of 16)
+    int num_splits;   // ceil(span / chunk)
+};
+// Returns false on invalid arguments.
+bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seq_len,
+                 int sliding_window, int num_splits_request, DecodePlan *plan);
+size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p);
+
+struct DecodeArgs {
+    void *out;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_table;
+    int max_num_blocks;
+    const int32_t *seq_lens;
+    int batch;
+    int max_seq_len;
+    int64_t num_blocks;
+    int block_size;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int sliding_window;
+    float scale;
+    void *workspace;
+    unsigned *err;
+};
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// ---------------------------------------------------------------- prefill ---
+struct PrefillArgs {
+    void *out;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *cu_seqlens_q;
+    const int32_t *cu_seqlens_k;  // may be null
+    const int32_t *seq_lens;      // may be null (then cu_seqlens_k is used)
+    const int32_t *block_table;
+    int max_num_blocks;
+    int num_seqs;
+    int total_q;
+    int max_seqlen_q;
+    int max_seqlen_k;
+    int64_t num_blocks;
+    int block_size;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int sliding_window;
+    float scale;
+    unsigned *err;
+};
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace pa

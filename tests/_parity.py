@@ -1,0 +1,72 @@
+"""Helpers shared by the GPU parity tests: run the oracle on host copies of a case's
+inputs and compare the library's bf16 outputs with the oracle's fp64 results."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_attention_03_gb300.inputs import PagedCase, bf16_bits
+
+# The stated bar for bf16-in / fp32-accumulate attention against the fp64 oracle.
+MAX_ABS = 1e-2
+MEAN_ABS = 1e-3
+
+
+def host_inputs(case: PagedCase) -> dict:
+    """uint16 copies of every bf16 input (taken before any kernel touches the cache)."""
+    return dict(q=bf16_bits(case.q), key=bf16_bits(case.key), value=bf16_bits(case.value),
+                k_cache=bf16_bits(case.k_cache), v_cache=bf16_bits(case.v_cache))
+
+
+def oracle_store(case: PagedCase, h: dict) -> None:
+    """Apply the step's store to the host cache copies (in place)."""
+    oracle.store_kvcache(h["key"], h["value"], h["k_cache"], h["v_cache"], case.slot_mapping,
+                         case.workload.block_size)
+
+
+def oracle_attention(case: PagedCase, h: dict, seqs=None, window=None) -> np.ndarray:
+    """Oracle output for the rows of the sequences in `seqs` (all when None), packed
+    in sequence order; [rows, H, D] float64."""
+    w = case.workload
+    win = w.sliding_window if window is None else window
+    if seqs is None:
+        return oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], case.cu_seqlens_q,
+                                      case.seq_lens, case.block_table, w.num_heads,
+                                      w.num_kv_heads, win, w.final_scale)
+    seqs = np.asarray(seqs)
+    cu = case.cu_seqlens_q
+    rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs]) if len(seqs) else \
+        np.zeros(0, np.int64)
+    ql = case.query_lens[seqs]
+    sub_cu = np.zeros(len(seqs) + 1, np.int32)
+    sub_cu[1:] = np.cumsum(ql)
+    return oracle.paged_attention(np.ascontiguousarray(h["q"][rows]), h["k_cache"],
+                                  h["v_cache"], sub_cu, case.seq_lens[seqs],
+                                  np.ascontiguousarray(case.block_table[seqs]), w.num_heads,
+                                  w.num_kv_heads, win, w.final_scale)
+
+
+def rows_of(case: PagedCase, seqs) -> np.ndarray:
+    cu = case.cu_seqlens_q
+    return np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
+
+
+def assert_parity(got: torch.Tensor, ref: np.ndarray, what: str = "",
+                  max_abs: float = MAX_ABS, mean_abs: float = MEAN_ABS) -> dict:
+    g = got.detach().float().cpu().double().numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    stats = {"max_abs": float(err.max()) if err.size else 0.0,
+             "mean_abs": float(err.mean()) if err.size else 0.0}
+    assert stats["max_abs"] <= max_abs, f"{what}: max-abs {stats['max_abs']:.3e} > {max_abs}"
+    assert stats["mean_abs"] <= mean_abs, f"{what}: mean-abs {stats['mean_abs']:.3e} > {mean_abs}"
+    return stats
+
+
+def device_tensors(case: PagedCase, device) -> dict:
+    """int32 metadata of the case as device tensors."""
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=device)
+    return dict(cu_seqlens_q=t(case.cu_seqlens_q), seq_lens=t(case.seq_lens),
+                block_table=t(case.block_table), slot_mapping=t(case.slot_mapping))
