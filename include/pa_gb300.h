@@ -148,6 +148,38 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
                     void *stream);
 
 /*
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this is a calling convention of this library only.
+ *
+ * Some callers have no way to call cudaMalloc: a plugin whose host framework hands it
+ * just the tensors of the call and owns every other byte of the GPU, a binding from a
+ * language without a device allocator, or a latency-critical loop that cannot pay for
+ * cudaMalloc/cudaFree's implicit device-wide synchronisation.  This entry point takes
+ * the same arguments as pa_decode minus the workspace and computes the same result;
+ * its split-K scratch is a fixed PA_NOALLOC_SCRATCH_BYTES array compiled into the
+ * library, which every GPU that loads the library holds until the process exits.
+ *
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Set-up: the first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream capture.
+ *   - Limit: returns PA_ERR_UNSUPPORTED, launching nothing, when the split-K
+ *     workspace these arguments need (pa_decode_workspace_size) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES; lower num_splits or the batch to fit.
+ *   - Sharing: all calls on a device share the one array and it keeps the last call's
+ *     partials.  Nothing in it needs to start at zero, but two calls that can overlap
+ *     on the GPU (different streams without ordering between them) race on it: order
+ *     them, or use pa_decode with a workspace per stream.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+pa_status pa_decode_noalloc(void *out, const void *q, const void *key, const void *value,
+                            const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *block_table, int max_num_blocks,
+                            const int32_t *seq_lens, int batch, int max_seq_len,
+                            int64_t num_blocks, int block_size, int num_heads,
+                            int num_kv_heads, int head_dim, int sliding_window, float scale,
+                            int num_splits, void *stream);
+
+/*
  * pa_varlen_prefill - packed variable-length causal / chunked prefill over the
  * paged cache.  "MinivLLM API docs - Attention", section flash_attention_prefill
  * (varlen packing by cu_seqlens, causal, GQA); "vllm-npu 0.4.2, xformers.py",

@@ -22,6 +22,7 @@ from ._lib import (  # noqa: F401
     library_path,
     load,
     pa_decode,
+    pa_decode_noalloc,
     pa_decode_num_splits,
     pa_decode_workspace_size,
     pa_read_device_error,

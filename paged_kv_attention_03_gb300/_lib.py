@@ -27,7 +27,7 @@ DEVERR_SEQLENS_K = 0x10
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
-            "pa_read_device_error")
+            "pa_read_device_error", "pa_decode_noalloc")
 
 
 class PAError(RuntimeError):
@@ -225,3 +225,42 @@ def pa_read_device_error(clear: bool = True, device: torch.device | None = None)
     if st not in (PA_OK, PA_ERR_DEVICE_CHECK):
         raise PAError(st, "pa_read_device_error")
     return int(flags.value)
+
+
+def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                      scale: float, sliding_window: int = 0, num_splits: int = 0,
+                      key: torch.Tensor | None = None, value: torch.Tensor | None = None,
+                      slot_mapping: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """pa_decode without a workspace, for callers that cannot allocate device memory.
+
+    The split-K scratch is the library's own fixed per-device array, so no workspace is
+    allocated here; pass `out` to allocate nothing at all.  Calls that may overlap on
+    the GPU share that array and race; see include/pa_gb300.h.
+    """
+    lib = load()
+    fn = lib.pa_decode_noalloc
+    if fn.restype is not ctypes.c_int or fn.argtypes is None:
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64, i32, i32, i32,
+                       i32, i32, f32, i32, vp]
+        fn.restype = ctypes.c_int
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    batch, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
+        raise ValueError("pa_decode_noalloc: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    st = fn(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+            _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+            int(max_seq_len), nb, bs, num_heads, hkv, head_dim, int(sliding_window),
+            float(scale), int(num_splits), _stream(dev))
+    _check(st, "pa_decode_noalloc")
+    return out
