@@ -67,6 +67,7 @@ typedef enum pa_status {
 #define PA_DEVERR_SEQ_RANGE 0x4u   /* seq_len > max_num_blocks*block_size or > max_seq_len */
 #define PA_DEVERR_QUERY_LEN 0x8u   /* prefill: query_len > seq_len, or > max_seqlen_q */
 #define PA_DEVERR_SEQLENS_K 0x10u  /* prefill: cu_seqlens_k differences disagree with seq_lens */
+#define PA_DEVERR_TIMEOUT 0x20u    /* a pipeline wait gave up (internal error; output undefined) */
 
 /* Human-readable name of a status code (static storage). */
 const char *pa_status_string(pa_status status);
@@ -137,7 +138,7 @@ size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int 
  *                 256-byte aligned (may be NULL when that size is 0); its contents
  *                 on entry do not matter
  * Supported: head_dim in {64, 128}; block_size a power of two in [1, 1024];
- * num_heads / num_kv_heads in [1, 64].
+ * num_heads / num_kv_heads in [1, 64]; batch <= 65535.
  */
 pa_status pa_decode(void *out, const void *q, const void *key, const void *value,
                     const int32_t *slot_mapping, void *k_cache, void *v_cache,
@@ -207,7 +208,8 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *key, const voi
  *   max_seqlen_q  host-side upper bound of sq_i (sizes the grid); larger is flagged
  *   max_seqlen_k  host-side upper bound of sk_i; larger is flagged
  * Supported: head_dim in {64, 128}; block_size a power of two in [16, 256];
- * num_heads / num_kv_heads in [1, 128].
+ * num_heads / num_kv_heads in [1, 128]; num_seqs <= 65535; num_blocks * block_size and
+ * total_q below 2^31.
  */
 pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
                             const int32_t *slot_mapping, void *k_cache, void *v_cache,

@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     DEVERR_SEQ_RANGE,
     DEVERR_SEQLENS_K,
     DEVERR_SLOT_RANGE,
+    DEVERR_TIMEOUT,
     EXPORTED,
     PA_ERR_CUDA,
     PA_ERR_DEVICE_CHECK,

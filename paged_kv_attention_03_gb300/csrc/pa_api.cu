@@ -133,6 +133,7 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
     if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size > 1024) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
+    if (batch > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per sequence
     const bool has_new = key || value || slot_mapping;
     if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
     if (batch == 0) return PA_OK;
@@ -197,6 +198,8 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
     if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per sequence
+    if (num_blocks * block_size > 0x7fffff00LL || total_q > 0x7fffff00) return PA_ERR_UNSUPPORTED;
     const bool has_new = key || value || slot_mapping;
     if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0) return PA_OK;

@@ -1,0 +1,188 @@
+"""pa_varlen_prefill on the GPU against the fp64 oracle (max-abs <= 1e-2, mean-abs <= 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_03_gb300 as pa
+from paged_kv_attention_03_gb300.inputs import (SMALL_WORKLOADS, WORKLOADS, Workload,
+                                                bf16_bits, make_case, make_case_from_lengths,
+                                                split_mixed)
+
+from _parity import (assert_parity, device_tensors, host_inputs, oracle_attention,
+                     oracle_store)
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(case, dev, window=None, fused_store=True, use_cu_k=False, both=False, out=None):
+    w = case.workload
+    win = w.sliding_window if window is None else window
+    m = device_tensors(case, dev)
+    key = value = slots = None
+    if fused_store:
+        key, value, slots = case.key, case.value, m["slot_mapping"]
+    cu_k = None
+    seq_lens = m["seq_lens"]
+    if use_cu_k or both:
+        cuk = np.zeros(case.num_seqs + 1, np.int32)
+        cuk[1:] = np.cumsum(case.seq_lens)
+        cu_k = torch.as_tensor(cuk, device=dev)
+        if not both:
+            seq_lens = None
+    return pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"], seq_lens,
+                                m["block_table"], case.max_query_len, case.max_seq_len,
+                                w.final_scale, win, cu_seqlens_k=cu_k, key=key, value=value,
+                                slot_mapping=slots, out=out)
+
+
+def _full_check(case, dev, window=None, **kw):
+    h = host_inputs(case)
+    oracle_store(case, h)
+    ref = oracle_attention(case, h, window=window)
+    out = _prefill(case, dev, window=window, **kw)
+    flags = pa.pa_read_device_error(device=dev)
+    assert flags == 0, f"device error bits {flags:#x}"
+    np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    return assert_parity(out, ref, case.workload.name)
+
+
+@pytest.mark.parametrize("name", ["varlen_prefill_small", "mixed_window_small"])
+def test_prefill_small_workloads(cuda, name):
+    _full_check(make_case(name, seed=41, device=cuda), cuda)
+
+
+def test_prefill_single_short_sequence(cuda):
+    w = Workload("one", 8, 2, 128, 16, ())
+    _full_check(make_case_from_lengths(w, [0], [1], seed=40, device=cuda), cuda)
+    _full_check(make_case_from_lengths(w, [0], [40], seed=40, device=cuda), cuda)
+
+
+@pytest.mark.parametrize("window", [0, 1, 7, 16, 100, 129, 300])
+def test_prefill_windows_and_chunks(cuda, window):
+    w = Workload("win", 32, 8, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 0, 37, 130, 500, 3], [1, 160, 64, 129, 31, 1], seed=42,
+                                  device=cuda)
+    _full_check(case, cuda, window=window)
+
+
+@pytest.mark.parametrize("H,Hkv,D", [(8, 8, 128), (32, 8, 128), (40, 8, 128), (16, 2, 64),
+                                     (64, 4, 128), (6, 3, 64), (128, 1, 64)])
+def test_prefill_group_sizes_and_head_dims(cuda, H, Hkv, D):
+    w = Workload("g", H, Hkv, D, 16, ())
+    case = make_case_from_lengths(w, [0, 5, 100], [150, 17, 33], seed=43, device=cuda)
+    _full_check(case, cuda)
+    _full_check(case, cuda, window=50)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 256])
+def test_prefill_block_sizes(cuda, bs):
+    w = Workload("bs", 16, 4, 128, bs, ())
+    case = make_case_from_lengths(w, [0, 33, 250], [200, 15, 70], seed=44, device=cuda)
+    _full_check(case, cuda)
+
+
+@pytest.mark.parametrize("lens", [[16], [128], [127], [129], [255], [256], [257]])
+def test_prefill_tile_edges(cuda, lens):
+    w = Workload("edge", 32, 8, 128, 16, ())
+    _full_check(make_case_from_lengths(w, [0] * len(lens), lens, seed=45, device=cuda), cuda)
+    _full_check(make_case_from_lengths(w, [x // 2 for x in lens], [max(1, x // 3) for x in lens],
+                                       seed=46, device=cuda), cuda)
+
+
+def test_prefill_cu_seqlens_k_instead_of_seq_lens(cuda):
+    case = make_case("mixed_window_small", seed=47, device=cuda)
+    _full_check(case, cuda, use_cu_k=True)
+
+
+def test_prefill_cu_seqlens_k_disagreeing_is_flagged(cuda):
+    case = make_case("varlen_prefill_small", seed=48, device=cuda)
+    m = device_tensors(case, cuda)
+    cuk = np.zeros(case.num_seqs + 1, np.int32)
+    cuk[1:] = np.cumsum(case.seq_lens) + 1  # off by one
+    w = case.workload
+    pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"], m["seq_lens"],
+                         m["block_table"], case.max_query_len, case.max_seq_len, w.final_scale,
+                         0, cu_seqlens_k=torch.as_tensor(cuk, device=cuda))
+    assert pa.pa_read_device_error(device=cuda) & pa.DEVERR_SEQLENS_K
+
+
+def test_prefill_bad_block_index_is_flagged_not_faulted(cuda):
+    w = Workload("bad", 8, 2, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 0], [70, 40], seed=49, device=cuda)
+    m = device_tensors(case, cuda)
+    bt = case.block_table.copy()
+    bt[0, 2] = case.num_blocks + 7
+    pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"], m["seq_lens"],
+                         torch.as_tensor(bt, device=cuda), case.max_query_len, case.max_seq_len,
+                         w.final_scale, 0)
+    assert pa.pa_read_device_error(device=cuda) & pa.DEVERR_BLOCK_RANGE
+
+
+def test_prefill_query_longer_than_keys_is_flagged(cuda):
+    w = Workload("ql", 8, 2, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 10], [20, 5], seed=50, device=cuda)
+    m = device_tensors(case, cuda)
+    bad = torch.as_tensor(np.array([10, 15], np.int32), device=cuda)  # 20 queries, 10 keys
+    pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"], bad,
+                         m["block_table"], 20, 20, w.final_scale, 0)
+    assert pa.pa_read_device_error(device=cuda) & pa.DEVERR_QUERY_LEN
+
+
+def test_prefill_stale_rows_past_the_sequence_are_ignored(cuda):
+    # Poison every cache slot past each sequence's end with NaN: the result must not change.
+    w = Workload("nan", 8, 2, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 20], [37, 3], seed=51, device=cuda)
+    h = host_inputs(case)
+    oracle_store(case, h)
+    ref = oracle_attention(case, h)
+    m = device_tensors(case, cuda)
+    pa.pa_store_kvcache(case.key, case.value, case.k_cache, case.v_cache, m["slot_mapping"])
+    for i in range(case.num_seqs):
+        sk = int(case.seq_lens[i])
+        last = int(case.block_table[i, (sk - 1) // 16])
+        if sk % 16:
+            case.k_cache[last, sk % 16:] = float("nan")
+            case.v_cache[last, sk % 16:] = float("nan")
+    out = pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"],
+                               m["seq_lens"], m["block_table"], case.max_query_len,
+                               case.max_seq_len, w.final_scale, 0)
+    assert_parity(out, ref)
+
+
+def _sampled_rows_check(case, dev, seqs, n_rows=24, seed=0):
+    """Run the whole-batch prefill (launch configuration of the benchmark) and compare
+    sampled rows of the given sequences with the oracle, row by row."""
+    w = case.workload
+    h = host_inputs(case)
+    oracle_store(case, h)
+    out = _prefill(case, dev)
+    flags = pa.pa_read_device_error(device=dev)
+    assert flags == 0, f"device error bits {flags:#x}"
+    rng = np.random.default_rng(seed)
+    got, ref = [], []
+    for i in seqs:
+        a, b = int(case.cu_seqlens_q[i]), int(case.cu_seqlens_q[i + 1])
+        sq, sk = b - a, int(case.seq_lens[i])
+        rows = sorted(set([0, sq - 1, min(sq - 1, 127), min(sq - 1, 128)] +
+                          list(rng.integers(0, sq, size=n_rows))))
+        for r in rows:
+            ref.append(oracle.attend_row(h["q"][a + r], h["k_cache"], h["v_cache"],
+                                         case.block_table[i], sk, sk - sq + r, w.num_heads,
+                                         w.num_kv_heads, w.sliding_window, w.final_scale))
+            got.append(out[a + r])
+    return assert_parity(torch.stack(got), np.stack(ref))
+
+
+def test_prefill_full_size_varlen(cuda):
+    # 16 prompts of U[128, 2048] tokens, 32/8 heads, D=128, bs=16: the benchmark's launch.
+    case = make_case("varlen_prefill", seed=0, device=cuda)
+    order = np.argsort(case.query_lens)
+    _sampled_rows_check(case, cuda, [order[0], order[7], order[-1]])
+
+
+def test_prefill_full_size_mixed_chunks(cuda):
+    # 8 chunks of 512 over contexts U[1024, 8192] + 128 decodes, window 4096, in one call.
+    case = make_case("mixed_window", seed=0, device=cuda)
+    pre, dec = split_mixed(case)
+    _sampled_rows_check(case, cuda, [pre[0], pre[3], pre[-1], dec[0], dec[-1]], n_rows=12)
