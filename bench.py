@@ -386,6 +386,9 @@ def main():
                     choices=["batched_decode", "long_decode", "tiny_decode", "mixed_window"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
+                    help="decode: the decode step only; prefill: the prefill step only "
+                         "(profiling runs); both: the full JSON line")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     rank, local, ws = _dist()
@@ -400,6 +403,12 @@ def main():
     pa.build()
     pa.load()
     peaks = _peaks()
+    if args.leg == "prefill":
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        res = _prefill_leg(pa, dev, rank, peaks, flush, torch.cuda.current_stream(dev), args)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     wl = WORKLOADS[args.workload]
     # Weak scaling: every rank runs its own replica (own seed), no data-path collective.
     case = make_case(wl, seed=rank, device=dev)
@@ -433,6 +442,12 @@ def main():
     ms_per_step = total_ms / args.steps
     attn_mean = statistics.mean(attn_ms)
     achieved = runner.work / (attn_mean / 1e3) / 1e9
+
+    if args.leg == "decode":
+        if rank == 0:
+            print(json.dumps({"decode_gbs": round(value, 2), "attention_gbs": round(achieved, 2),
+                              "ms_per_step": ms_per_step}), flush=True)
+        return
 
     e2e = None
     if not args.no_e2e:

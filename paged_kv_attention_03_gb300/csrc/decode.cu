@@ -27,10 +27,13 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace pa {
 
 namespace {
+
+using sm100::ex2_approx;
 
 struct DecodeKernelParams {
     __nv_bfloat16 *out;
@@ -82,7 +85,7 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
 }
 
 template <int D, int NWARPS, int NSTAGES>
-__global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const DecodeKernelParams p) {
+__global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const DecodeKernelParams p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
@@ -142,39 +145,63 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const Deco
     const uint32_t stage_base = smem_u32(my_stages);
     const uint64_t policy = l2_policy_evict_first();
 
+    // With block_size >= 16 a 16-key unit never straddles two blocks: one table lookup
+    // per unit and fixed row strides.  Smaller blocks take the per-row path.
+    const bool page_units = p.log2_bs >= 4;
+    const int64_t row_stride = static_cast<int64_t>(p.num_kv_heads) * D;
+
     auto issue = [&](int u, int st) {
         const uint32_t sb = stage_base + st * STAGE_BYTES;
         const int c = lane % CPR;
         const int rsub = lane / CPR;
+        const int j0 = u * 16;
+        if (page_units) {
+            const bool full = j0 >= lo && j0 + 16 <= hi;
+            const int blk = __ldg(bt_row + (j0 >> p.log2_bs));
+            const bool blk_ok = blk >= 0 && blk < p.num_blocks;
+            if (!blk_ok && lane == 0) flag_error(p.err, kErrBlockRange);
+            const int64_t base =
+                blk_ok ? (((static_cast<int64_t>(blk) << p.log2_bs) + (j0 & bs_mask)) *
+                              p.num_kv_heads + kvh) * D + c * 8
+                       : 0;
 #pragma unroll
-        for (int i = 0; i < PASSES; ++i) {
-            const int r = i * ROWS_PER_PASS + rsub;
-            const int j = u * 16 + r;
-            const __nv_bfloat16 *ksrc = p.k_cache;
-            const __nv_bfloat16 *vsrc = p.v_cache;
-            uint32_t nbytes = 0;
-            if (j >= lo && j < hi) {
-                const int blk = __ldg(bt_row + (j >> p.log2_bs));
-                if (blk < 0 || blk >= p.num_blocks) {
-                    flag_error(p.err, kErrBlockRange);
-                } else {
-                    const int64_t off =
-                        (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
-                             p.num_kv_heads + kvh) * D + c * 8;
-                    ksrc = p.k_cache + off;
-                    vsrc = p.v_cache + off;
-                    nbytes = 16;
-                }
+            for (int i = 0; i < PASSES; ++i) {
+                const int r = i * ROWS_PER_PASS + rsub;
+                const bool ok = blk_ok && (full || (j0 + r >= lo && j0 + r < hi));
+                const int64_t off = ok ? base + r * row_stride : 0;
+                const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
+                cp_async_16_policy(sb + so, p.k_cache + off, ok ? 16u : 0u, policy);
+                cp_async_16_policy(sb + TILE_BYTES + so, p.v_cache + off, ok ? 16u : 0u, policy);
             }
-            const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
-            cp_async_16_policy(sb + so, ksrc, nbytes, policy);
-            cp_async_16_policy(sb + TILE_BYTES + so, vsrc, nbytes, policy);
+        } else {
+#pragma unroll
+            for (int i = 0; i < PASSES; ++i) {
+                const int r = i * ROWS_PER_PASS + rsub;
+                const int j = j0 + r;
+                int64_t off = 0;
+                uint32_t nbytes = 0;
+                if (j >= lo && j < hi) {
+                    const int blk = __ldg(bt_row + (j >> p.log2_bs));
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        flag_error(p.err, kErrBlockRange);
+                    } else {
+                        off = (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
+                                   p.num_kv_heads + kvh) * D + c * 8;
+                        nbytes = 16;
+                    }
+                }
+                const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
+                cp_async_16_policy(sb + so, p.k_cache + off, nbytes, policy);
+                cp_async_16_policy(sb + TILE_BYTES + so, p.v_cache + off, nbytes, policy);
+            }
         }
     };
 
     float o[DTILES][4];
 #pragma unroll
     for (int i = 0; i < DTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    // m_run is the reference maximum the weights are taken against: it only moves when
+    // the true maximum exceeds it by more than 2^8, so O is rarely rescaled.
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
 
@@ -200,8 +227,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const Deco
         const uint32_t kb = stage_base + (it % NSTAGES) * STAGE_BYTES;
         const uint32_t vb = kb + TILE_BYTES;
 
-        // S = Q K^T for 16 keys: two n-tiles of 8 keys.
+        // S = Q K^T for 16 keys: two n-tiles of 8 keys, even and odd k-steps in
+        // separate accumulators to halve the dependent MMA chain.
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
             const int r = ((lane >> 4) << 3) + (lane & 7);
             const int chi = (lane >> 3) & 1;
@@ -210,60 +239,79 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const Deco
                 uint32_t kf[4];
                 const int ch = 2 * ks + chi;
                 ldmatrix_x4(kf, kb + r * ROWB + ((ch ^ (r & 7)) << 4));
-                mma_bf16_16816(s[0], qa[ks], kf[0], kf[1]);
-                mma_bf16_16816(s[1], qa[ks], kf[2], kf[3]);
+                if (ks & 1) {
+                    mma_bf16_16816(s2[0], qa[ks], kf[0], kf[1]);
+                    mma_bf16_16816(s2[1], qa[ks], kf[2], kf[3]);
+                } else {
+                    mma_bf16_16816(s[0], qa[ks], kf[0], kf[1]);
+                    mma_bf16_16816(s[1], qa[ks], kf[2], kf[3]);
+                }
             }
         }
 
-        // Mask, online softmax (rows lane/4 and lane/4 + 8 of the head tile).
+        // Scale, mask (edge units only), online softmax on rows lane/4 and lane/4 + 8.
+        const bool edge = u * 16 < lo || u * 16 + 16 > hi;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int j = u * 16 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                const float v = (j >= lo && j < hi) ? s[nt][e] * p.scale_log2 : -INFINITY;
+                float v = (s[nt][e] + s2[nt][e]) * p.scale_log2;
+                if (edge) {
+                    const int j = u * 16 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                    if (j < lo || j >= hi) v = -INFINITY;
+                }
                 s[nt][e] = v;
                 mx[e >> 1] = fmaxf(mx[e >> 1], v);
             }
         }
-        float corr[2];
+        bool need[2];
+        float m_new[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
             mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-            const float m_new = fmaxf(m_run[i], mx[i]);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            corr[i] = exp2f(m_run[i] - m_use);
-            m_run[i] = m_new;
-            mx[i] = m_use;
+            m_new[i] = fmaxf(m_run[i], mx[i]);
+            need[i] = m_new[i] > m_run[i] + 8.f;
         }
-        float rowsum[2] = {0.f, 0.f};
+        if (__any_sync(0xffffffffu, need[0] || need[1])) {
+            float f[2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+            for (int i = 0; i < 2; ++i) {
+                f[i] = need[i] ? ex2_approx(m_run[i] - m_new[i]) : 1.f;
+                l_run[i] *= f[i];
+                if (need[i]) m_run[i] = m_new[i];
+            }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float pv = exp2f(s[nt][e] - mx[e >> 1]);
-                s[nt][e] = pv;
-                rowsum[e >> 1] += pv;
+            for (int dt = 0; dt < DTILES; ++dt) {
+                o[dt][0] *= f[0];
+                o[dt][1] *= f[0];
+                o[dt][2] *= f[1];
+                o[dt][3] *= f[1];
             }
         }
-        l_run[0] = l_run[0] * corr[0] + rowsum[0];
-        l_run[1] = l_run[1] * corr[1] + rowsum[1];
+        const float m_use0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float m_use1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
-        for (int dt = 0; dt < DTILES; ++dt) {
-            o[dt][0] *= corr[0];
-            o[dt][1] *= corr[0];
-            o[dt][2] *= corr[1];
-            o[dt][3] *= corr[1];
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = ex2_approx(s[nt][0] - m_use0);
+            s[nt][1] = ex2_approx(s[nt][1] - m_use0);
+            s[nt][2] = ex2_approx(s[nt][2] - m_use1);
+            s[nt][3] = ex2_approx(s[nt][3] - m_use1);
         }
-
-        // O += P V (P as the A operand straight from the S accumulators).
+        // P as the A operand straight from the S accumulators; the denominator sums the
+        // bf16 weights the MMA actually uses.
         uint32_t pa[4];
         pa[0] = pack_bf16x2(s[0][0], s[0][1]);
         pa[1] = pack_bf16x2(s[0][2], s[0][3]);
         pa[2] = pack_bf16x2(s[1][0], s[1][1]);
         pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+        l_run[0] += __uint_as_float(pa[0] << 16) + __uint_as_float(pa[0] & 0xffff0000u) +
+                    __uint_as_float(pa[2] << 16) + __uint_as_float(pa[2] & 0xffff0000u);
+        l_run[1] += __uint_as_float(pa[1] << 16) + __uint_as_float(pa[1] & 0xffff0000u) +
+                    __uint_as_float(pa[3] << 16) + __uint_as_float(pa[3] & 0xffff0000u);
+
+        // O += P V.
         {
             const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
             const int chi = lane >> 4;
@@ -321,7 +369,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) decode_split_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < NWARPS; ++w) {
             const float mw = m_s[w * 16 + row];
-            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            const float f = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
             L += f * l_s[w * 16 + row];
             acc += f * o_s[(w * 16 + row) * OSTRIDE + d];
         }
@@ -369,7 +417,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
     for (int s = 0; s < nsplit; ++s) {
-        const float w = ml[2 * s + 1] * exp2f(ml[2 * s] - M);
+        const float w = ml[2 * s + 1] * ex2_approx(ml[2 * s] - M);
         wsum += w;
         const float *src = os + static_cast<int64_t>(s) * D;
         if constexpr (PER_LANE == 4) {
@@ -391,7 +439,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
 }
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 4;
+constexpr int kDecodeStages = 3;
 
 template <int D>
 constexpr int decode_smem_bytes() {

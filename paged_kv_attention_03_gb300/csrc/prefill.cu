@@ -438,14 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c8 = 0; c8 < BN / 8; ++c8) {
                 float e[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    e[i] = ex2_approx(s[c8 * 8 + i] - m_use);
-                    l_sum += e[i];
+                for (int i = 0; i < 8; ++i) e[i] = ex2_approx(s[c8 * 8 + i] - m_use);
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pk[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
+                    // The denominator sums the bf16 weights the MMA actually uses.
+                    l_sum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
                 }
                 const uint32_t addr = sP + (c8 >> 3) * HALF + row * 128 +
                                       ((((c8 & 7) ^ (row & 7))) << 4);
-                st_shared_v4(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                             pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+                st_shared_v4(addr, pk[0], pk[1], pk[2], pk[3]);
             }
             // Keys of the sequence's last, partly filled 16-key piece that lie past sk
             // are stale cache rows: zero them in the V tile so 0 * V stays 0.
