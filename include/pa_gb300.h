@@ -207,6 +207,7 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *key, const voi
  *   block_table   [num_seqs, max_num_blocks] int32, device
  *   max_seqlen_q  host-side upper bound of sq_i (sizes the grid); larger is flagged
  *   max_seqlen_k  host-side upper bound of sk_i; larger is flagged
+ * scale must be positive and finite (PA_ERR_INVALID_ARG otherwise).
  * Supported: head_dim in {64, 128}; block_size a power of two in [16, 256];
  * num_heads / num_kv_heads in [1, 128]; num_seqs <= 65535; num_blocks * block_size and
  * total_q below 2^31.

@@ -13,7 +13,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/pa_gb300.h"
+#include "pa_gb300.h"
 
 namespace {
 

@@ -7,7 +7,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/pa_gb300.h"
+#include "pa_gb300.h"
 #include "pa_internal.h"
 
 namespace {
@@ -195,6 +195,7 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
         return PA_ERR_INVALID_ARG;
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (max_seqlen_q > max_seqlen_k) return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return PA_ERR_INVALID_ARG;  // folded into exp2
     if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 128) return PA_ERR_UNSUPPORTED;

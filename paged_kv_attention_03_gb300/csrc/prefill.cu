@@ -10,26 +10,32 @@
 //
 // GB300 design (the page's Triton kernel uses 32x32 or 64x64 tiles sized for ~48 KB of
 // shared memory and reads contiguous K/V):
-//  * One CTA per (128-row query tile, kv head, sequence).  The 128 MMA rows pack the G
+//  * Work item = (128-row query tile, kv head, sequence).  The 128 MMA rows pack the G
 //    query heads of one kv head for T = floor(128 / G) consecutive tokens (row m =
 //    token m / G, head m % G), so one K/V tile feeds all heads of the group.
-//  * K/V come straight from the paged cache: the TMA producer walks block_table and
-//    fetches each 16-key piece of a page as one 3-D box {64 dims, 1 kv head, 16 rows}
-//    with 128-byte swizzle; pieces past the sequence are loaded from an out-of-range
+//  * Persistent CTAs, one per SM, walk the items round-robin, longest query tiles
+//    first; the load / MMA / softmax pipelines run on across item boundaries (Q is
+//    double-buffered, every ring barrier counts tiles globally).
+//  * K/V come straight from the paged cache: the TMA producers walk block_table and
+//    fetch each 16-key piece of a page as one 3-D box {64 dims, 1 kv head, 16 rows}
+//    with 128-byte swizzle; pieces past the sequence come from an out-of-range
 //    coordinate, which the TMA unit fills with zeros.
-//  * S = Q K^T (M=128, N=128 keys, K=head_dim) and O += P V (M=128, N=head_dim,
-//    K=128 keys) run as tcgen05.mma kind::f16 with fp32 accumulators in tensor memory:
-//    S double-buffered (2 x 128 columns), O in 128 columns.
+//  * S = Q K^T (M=128, N=128 keys, K=head_dim) runs as tcgen05.mma kind::f16 with both
+//    operands in shared memory and the fp32 accumulator in tensor memory (two S buffers
+//    of 128 columns).  The softmax writes P as bf16 back into the first 64 columns of
+//    the same buffer, and O += P V (M=128, N=head_dim, K=128 keys) takes P straight
+//    from tensor memory, V from shared memory (N-major), O in 128 columns.
 //  * Warp roles: warp 0 loads Q and K, warp 6 loads V, warp 1 issues the MMAs (one
-//    thread), warps 2-5 own one accumulator row each (thread = TMEM lane) and do the
-//    mask, the online softmax in base 2 (the O rescale in TMEM is skipped unless the
-//    running max grows by more than 2^8), write P as bf16 to shared memory, and the
-//    epilogue.
-//  * Every mbarrier wait is bounded: on timeout the CTA raises an error bit, drains, frees
-//    its tensor memory and returns.
+//    thread), warps 2-5 own one accumulator row each (thread = TMEM lane): mask, online
+//    softmax in base 2 with the scale folded into the exponent, lazy O rescale (only
+//    when the running max grows by more than 2^8, so the softmax rarely waits for the
+//    previous P V), and the epilogue.
+//  * Every mbarrier wait is bounded: on timeout the CTA raises an error bit, drains,
+//    frees its tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -46,12 +52,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128;                       // MMA rows per CTA
-constexpr int BN = 128;                       // keys per KV tile
-constexpr uint32_t HALF = 128u * 128u;        // [128 rows][64 bf16] = 16 KB (one swizzle span)
-constexpr int NSK = 3;                        // K stages
-constexpr int NSV = 2;                        // V stages
-constexpr int kThreads = 224;                 // 7 warps
+constexpr int BM = 128;                  // MMA rows per work item
+constexpr int BN = 128;                  // keys per KV tile
+constexpr uint32_t HALF = 128u * 128u;   // [128 rows][64 bf16] = 16 KB (one swizzle span)
+constexpr int NSK = 3;                   // K stages
+constexpr int NSV = 2;                   // V stages
+constexpr int kThreads = 224;            // 7 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -68,6 +74,8 @@ struct PrefillKernelParams {
     int max_num_blocks;
     int num_seqs;
     int max_seqlen_q;
+    int q_tiles;  // ceil(max_seqlen_q / tok_per_tile)
+    int n_items;  // q_tiles * num_kv_heads * num_seqs
     int64_t seq_cap;  // max_num_blocks * block_size, capped by max_seqlen_k
     int64_t num_blocks;
     int log2_bs;
@@ -76,38 +84,82 @@ struct PrefillKernelParams {
     int group;
     int tok_per_tile;  // floor(128 / group)
     int window;
-    float scale_log2;
+    float scale_log2;  // scale * log2(e) > 0
     unsigned *err;
 };
 
 // Barrier indices.
 enum : int {
-    B_Q = 0,
-    B_KFULL = 1,
+    B_QFULL = 0,
+    B_QEMPTY = B_QFULL + 2,
+    B_KFULL = B_QEMPTY + 2,
     B_KEMPTY = B_KFULL + NSK,
     B_VFULL = B_KEMPTY + NSK,
     B_VEMPTY = B_VFULL + NSV,
     B_SFULL = B_VEMPTY + NSV,
-    B_SFREE = B_SFULL + 2,
-    B_PFULL = B_SFREE + 2,
-    B_ODONE = B_PFULL + 1,
-    NBARS = B_ODONE + 1
+    B_PFULL = B_SFULL + 2,  // one per S buffer (tile parity)
+    B_ODONE = B_PFULL + 2,  // one per S buffer: keeps every waiter within one phase
+    NBARS = B_ODONE + 2
 };
 
 template <int HD>
 struct Layout {
     static constexpr int NHALF = HD / 64;
     static constexpr uint32_t TILE = NHALF * HALF;  // one [128][HD] bf16 tile
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + TILE;
+    static constexpr uint32_t OFF_Q = 0;             // two Q buffers
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
-    static constexpr uint32_t OFF_P = OFF_V + NSV * TILE;
-    static constexpr uint32_t OFF_BAR = OFF_P + 2 * HALF;  // P is [128][128 keys]
+    static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr uint32_t BYTES = OFF_MISC + 16;
-    // Request at least 116 KB so a single CTA owns an SM (and all of its TMEM).
+    // At least 116 KB so a single CTA owns an SM (and all of its TMEM).
     static constexpr uint32_t SMEM = (BYTES + 1024 > 118784u ? BYTES + 1024 : 118784u);
 };
+
+// Geometry of one work item; every role derives it identically.
+struct Item {
+    bool valid;
+    int seq, kvh, q0, rows_tok, q_start, sq, sk, kt0, n_tiles;
+};
+
+__device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, bool report) {
+    Item it;
+    const int per_qt = p.num_kv_heads * p.num_seqs;
+    const int qt = p.q_tiles - 1 - idx / per_qt;  // longest-running tiles first
+    const int rem = idx - (idx / per_qt) * per_qt;
+    it.seq = rem / p.num_kv_heads;
+    it.kvh = rem - it.seq * p.num_kv_heads;
+    it.valid = false;
+    it.q_start = p.cu_q[it.seq];
+    it.sq = p.cu_q[it.seq + 1] - it.q_start;
+    int sk;
+    if (p.seq_lens != nullptr) {
+        sk = p.seq_lens[it.seq];
+        if (report && p.cu_k != nullptr && p.cu_k[it.seq + 1] - p.cu_k[it.seq] != sk)
+            flag_error(p.err, kErrSeqlensK);
+    } else {
+        sk = p.cu_k[it.seq + 1] - p.cu_k[it.seq];
+    }
+    if (sk < 0 || static_cast<int64_t>(sk) > p.seq_cap) {
+        if (report) flag_error(p.err, kErrSeqRange);
+        sk = sk < 0 ? 0 : static_cast<int>(p.seq_cap);
+    }
+    it.sk = sk;
+    if (it.sq < 0 || it.sq > sk || it.sq > p.max_seqlen_q) {
+        if (report) flag_error(p.err, kErrQueryLen);
+        if (it.sq < 0 || it.sq > sk) return it;
+    }
+    it.q0 = qt * p.tok_per_tile;
+    if (it.q0 >= it.sq) return it;
+    it.rows_tok = min(p.tok_per_tile, it.sq - it.q0);
+    const int p_lo = sk - it.sq + it.q0;
+    const int p_hi = p_lo + it.rows_tok - 1;
+    const int kmin = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
+    it.kt0 = kmin / BN;
+    it.n_tiles = p_hi / BN - it.kt0 + 1;
+    it.valid = true;
+    return it;
+}
 
 // Bounded wait by one thread.
 __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -163,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillKernelParams p) {
     using L = Layout<HD>;
     constexpr int NHALF = L::NHALF;
-    constexpr int KSTEPS_S = HD / 16;   // MMAs per S tile
-    constexpr int KSTEPS_O = BN / 16;   // MMAs per PV tile
+    constexpr int KSTEPS_S = HD / 16;  // MMAs per S tile
+    constexpr int KSTEPS_O = BN / 16;  // MMAs per PV tile
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -173,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base + L::OFF_Q;
     const uint32_t sK = base + L::OFF_K;
     const uint32_t sV = base + L::OFF_V;
-    const uint32_t sP = base + L::OFF_P;
     const uint32_t sBar = base + L::OFF_BAR;
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sb + L::OFF_MISC);
@@ -181,45 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int seq = blockIdx.z;
-    const int kvh = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest-running tiles first
-    const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0;
-
-    // ---- sequence geometry (uniform over the CTA) ----
-    const int q_start = p.cu_q[seq];
-    const int sq = p.cu_q[seq + 1] - q_start;
-    int sk;
-    if (p.seq_lens != nullptr) {
-        sk = p.seq_lens[seq];
-        if (p.cu_k != nullptr && reporter && p.cu_k[seq + 1] - p.cu_k[seq] != sk)
-            flag_error(p.err, kErrSeqlensK);
-    } else {
-        sk = p.cu_k[seq + 1] - p.cu_k[seq];
-    }
-    if (sk < 0 || static_cast<int64_t>(sk) > p.seq_cap) {
-        if (reporter) flag_error(p.err, kErrSeqRange);
-        sk = sk < 0 ? 0 : static_cast<int>(p.seq_cap);
-    }
-    if (sq < 0 || sq > sk || sq > p.max_seqlen_q) {
-        if (reporter) flag_error(p.err, kErrQueryLen);
-        if (sq < 0 || sq > sk) return;
-    }
-    const int T = p.tok_per_tile;
     const int G = p.group;
-    const int q0 = qt * T;
-    if (q0 >= sq) return;
-    const int rows_tok = min(T, sq - q0);
-    const int p_lo = sk - sq + q0;
-    const int p_hi = p_lo + rows_tok - 1;
-    const int kmin = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
-    const int kt0 = kmin / BN;
-    const int kt1 = p_hi / BN;
-    const int n_tiles = kt1 - kt0 + 1;
 
     // ---- set-up: barriers, tensor memory ----
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_QFULL + s), 1);
+            mbar_init(bar(B_QEMPTY + s), 1);
+            mbar_init(bar(B_SFULL + s), 1);
+            mbar_init(bar(B_PFULL + s), 4);
+            mbar_init(bar(B_ODONE + s), 1);
+        }
         for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
             mbar_init(bar(B_KEMPTY + s), 1);
@@ -228,12 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_VEMPTY + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_SFREE + s), 4);
-        }
-        mbar_init(bar(B_PFULL), 4);
-        mbar_init(bar(B_ODONE), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -246,14 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    const int32_t *bt_row = p.block_table + static_cast<int64_t>(seq) * p.max_num_blocks;
     const int bs_mask = (1 << p.log2_bs) - 1;
-    // Cache row (slot) of the 16-key piece starting at key k0, or an out-of-range row
-    // (zero fill) when the piece is past the sequence or its block index is invalid.
-    auto kv_row = [&](int k0) -> int {
-        if (k0 >= sk) return -16;
-        const int blk = __ldg(bt_row + (k0 >> p.log2_bs));
+
+    // Cache row (slot) of the 16-key piece of `it` starting at key k0, or an
+    // out-of-range row (zero fill) past the sequence or for an invalid block index.
+    auto kv_row = [&](const Item &it, int k0) -> int {
+        if (k0 >= it.sk) return -16;
+        const int blk = __ldg(p.block_table + static_cast<int64_t>(it.seq) * p.max_num_blocks +
+                              (k0 >> p.log2_bs));
         if (blk < 0 || blk >= p.num_blocks) {
             flag_error(p.err, kErrBlockRange);
             return -16;
@@ -266,90 +283,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&p.tmap_q);
             prefetch_tmap(&p.tmap_k);
-            mbar_arrive_expect_tx(bar(B_Q), static_cast<uint32_t>(G * T) * 128u * NHALF);
-#pragma unroll
-            for (int h = 0; h < NHALF; ++h)
-                tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, kvh * G, q_start + q0, bar(B_Q));
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % NSK;
-                if (j >= NSK && !wait1(bar(B_KEMPTY + st), ((j / NSK) - 1) & 1, abort_flag, p.err))
+            uint32_t t = 0, ic = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+                const Item it = get_item(p, idx, false);
+                if (!it.valid) continue;
+                const int qb = ic & 1;
+                if (ic >= 2 && !wait1(bar(B_QEMPTY + qb), ((ic >> 1) - 1) & 1, abort_flag, p.err))
                     break;
-                const int key0 = (kt0 + j) * BN;
-                mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
-                const uint32_t dst = sK + st * L::TILE;
-#pragma unroll 1
-                for (int u = 0; u < BN / 16; ++u) {
-                    const int row = kv_row(key0 + u * 16);
+                mbar_arrive_expect_tx(bar(B_QFULL + qb),
+                                      static_cast<uint32_t>(G * p.tok_per_tile) * 128u * NHALF);
 #pragma unroll
-                    for (int h = 0; h < NHALF; ++h)
-                        tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_k, h * 64, kvh, row,
-                                    bar(B_KFULL + st));
+                for (int h = 0; h < NHALF; ++h)
+                    tma_load_3d(sQ + qb * L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                it.q_start + it.q0, bar(B_QFULL + qb));
+                for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                    const int st = t % NSK;
+                    if (t >= NSK &&
+                        !wait1(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int key0 = (it.kt0 + j) * BN;
+                    mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
+                    const uint32_t dst = sK + st * L::TILE;
+#pragma unroll 1
+                    for (int u = 0; u < BN / 16; ++u) {
+                        const int row = kv_row(it, key0 + u * 16);
+#pragma unroll
+                        for (int h = 0; h < NHALF; ++h)
+                            tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_k, h * 64, it.kvh, row,
+                                        bar(B_KFULL + st));
+                    }
                 }
+                ++ic;
             }
         }
     } else if (warp == 6) {
-        // ---------------- V producer ----------------
+        // ---------------- V producer (also reports per-sequence input errors) ----------------
         if (lane == 0) {
             prefetch_tmap(&p.tmap_v);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % NSV;
-                if (j >= NSV && !wait1(bar(B_VEMPTY + st), ((j / NSV) - 1) & 1, abort_flag, p.err))
-                    break;
-                const int key0 = (kt0 + j) * BN;
-                mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
-                const uint32_t dst = sV + st * L::TILE;
+            uint32_t t = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+                const Item it = get_item(p, idx, true);
+                if (!it.valid) continue;
+                for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                    const int st = t % NSV;
+                    if (t >= NSV &&
+                        !wait1(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int key0 = (it.kt0 + j) * BN;
+                    mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
+                    const uint32_t dst = sV + st * L::TILE;
 #pragma unroll 1
-                for (int u = 0; u < BN / 16; ++u) {
-                    const int row = kv_row(key0 + u * 16);
+                    for (int u = 0; u < BN / 16; ++u) {
+                        const int row = kv_row(it, key0 + u * 16);
 #pragma unroll
-                    for (int h = 0; h < NHALF; ++h)
-                        tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_v, h * 64, kvh, row,
-                                    bar(B_VFULL + st));
+                        for (int h = 0; h < NHALF; ++h)
+                            tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_v, h * 64, it.kvh, row,
+                                        bar(B_VFULL + st));
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // Order on the tensor pipe: S(t), P V(t-1), S(t+1), P V(t), ... across items.
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % NSK;
-                if (!wait1(bar(B_KFULL + st), (j / NSK) & 1, abort_flag, p.err)) return false;
-                const int sbuf = j & 1;
-                if (j >= 2 && !wait1(bar(B_SFREE + sbuf), ((j >> 1) - 1) & 1, abort_flag, p.err))
-                    return false;
-                tc_fence_after();
-                const uint32_t kbase = sK + st * L::TILE;
-#pragma unroll
-                for (int k = 0; k < KSTEPS_S; ++k) {
-                    const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sQ + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                    mma_bf16_ss(tmem + (sbuf ? kColS1 : kColS0), a, b, idesc_s, k > 0);
-                }
-                mma_commit(bar(B_SFULL + sbuf));
-                mma_commit(bar(B_KEMPTY + st));
-                return true;
-            };
-            bool ok = wait1(bar(B_Q), 0, abort_flag, p.err);
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-                const int st = j % NSV;
-                if (!wait1(bar(B_PFULL), j & 1, abort_flag, p.err)) break;
-                if (!wait1(bar(B_VFULL + st), (j / NSV) & 1, abort_flag, p.err)) break;
+            uint32_t t = 0, ic = 0;
+            bool ok = true;
+            bool have_prev = false;
+            uint32_t prev_t = 0;
+            bool prev_first = false;
+            auto issue_pv = [&](uint32_t tt, bool first) -> bool {
+                const int st = tt % NSV;
+                if (!wait1(bar(B_PFULL + (tt & 1)), (tt >> 1) & 1, abort_flag, p.err)) return false;
+                if (!wait1(bar(B_VFULL + st), (tt / NSV) & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
                 const uint32_t vbase = sV + st * L::TILE;
+                const uint32_t pcol = tmem + ((tt & 1) ? kColS1 : kColS0);
 #pragma unroll
                 for (int k = 0; k < KSTEPS_O; ++k) {
-                    const uint64_t a = smem_desc_sw128(sP + (k >> 2) * HALF + (k & 3) * 32, 16, 1024);
                     const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
-                    mma_bf16_ss(tmem + kColO, a, b, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                    mma_bf16_ts(tmem + kColO, pcol + k * 8, b, idesc_o,
+                                (!first || k > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_ODONE));
+                mma_commit(bar(B_ODONE + (tt & 1)));
                 mma_commit(bar(B_VEMPTY + st));
+                return true;
+            };
+            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+                const Item it = get_item(p, idx, false);
+                if (!it.valid) continue;
+                const int qb = ic & 1;
+                if (!wait1(bar(B_QFULL + qb), (ic >> 1) & 1, abort_flag, p.err)) break;
+                const uint32_t qbase = sQ + qb * L::TILE;
+                for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                    const int st = t % NSK;
+                    if (!wait1(bar(B_KFULL + st), (t / NSK) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = sK + st * L::TILE;
+                    const uint32_t scol = tmem + ((t & 1) ? kColS1 : kColS0);
+#pragma unroll
+                    for (int k = 0; k < KSTEPS_S; ++k) {
+                        const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
+                        const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
+                        mma_bf16_ss(scol, a, b, idesc_s, k > 0);
+                    }
+                    mma_commit(bar(B_SFULL + (t & 1)));
+                    mma_commit(bar(B_KEMPTY + st));
+                    if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY + qb));
+                    if (have_prev && !issue_pv(prev_t, prev_first)) {
+                        ok = false;
+                        break;
+                    }
+                    have_prev = true;
+                    prev_t = t;
+                    prev_first = j == 0;
+                }
+                ++ic;
             }
+            if (ok && have_prev) issue_pv(prev_t, prev_first);
         }
     } else {
         // ---------------- softmax / correction / epilogue (warps 2..5) ----------------
@@ -358,128 +421,130 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
         const int tok = row / G;
         const int g = row - tok * G;
-        const bool valid = tok < rows_tok;
-        const int pos = sk - sq + q0 + tok;
         const float sl2 = p.scale_log2;
         const int w = p.window;
-        float m_ref = -INFINITY;
-        float l_sum = 0.f;
+        uint32_t t = 0;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int sbuf = j & 1;
-            if (!wait_warp(bar(B_SFULL + sbuf), (j >> 1) & 1, abort_flag, p.err)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float s[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                tmem_ld_32x32b_x32(tmem + t_lane + (sbuf ? kColS1 : kColS0) + c * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SFREE + sbuf));
-
-            const int key0 = (kt0 + j) * BN;
-            const bool all_visible = key0 + BN - 1 <= pos && (w <= 0 || key0 >= pos - w + 1);
-            float mx = -INFINITY;
-            if (all_visible) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    s[c] *= sl2;
-                    mx = fmaxf(mx, s[c]);
-                }
-            } else {
-                const int lo = w > 0 ? pos - w + 1 : INT_MIN;
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const int k = key0 + c;
-                    const bool vis = k <= pos && k >= lo;
-                    s[c] = vis ? s[c] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, s[c]);
-                }
-            }
-            const float m_new = fmaxf(m_ref, mx);
-            const bool need = m_new > m_ref + 8.f;
-            if (j > 0) {
-                // PV(j-1) must be complete: O is stable and the P buffer is free.
-                if (!wait_warp(bar(B_ODONE), (j - 1) & 1, abort_flag, p.err)) {
+        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+            const Item it = get_item(p, idx, false);
+            if (!it.valid) continue;
+            const bool valid = tok < it.rows_tok;
+            const int pos = it.sk - it.sq + it.q0 + tok;
+            const int lo = w > 0 ? pos - w + 1 : INT_MIN;
+            float m_ref = -INFINITY;  // reference max (base-2 units) the weights use
+            float l_sum = 0.f;
+            for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                const int sbuf = t & 1;
+                const uint32_t scol = t_lane + (sbuf ? kColS1 : kColS0);
+                if (!wait_warp(bar(B_SFULL + sbuf), (t >> 1) & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
-                    const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < HD / 32; ++c) {
-                        float o[32];
-                        tmem_ld_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
-                        tmem_wait_ld();
+                float s[BN];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= f;
-                        tmem_st_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
-                    }
-                    tmem_wait_st();
-                    l_sum *= f;
-                    if (need) m_ref = m_new;
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(tmem + scol + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
                 }
-            } else {
-                m_ref = m_new;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                tmem_wait_ld();
 
-            // P = 2^(s - m) as bf16 into the swizzled K-major P tile; row sum in fp32.
+                const int key0 = (it.kt0 + j) * BN;
+                const bool all_visible = key0 + BN - 1 <= pos && key0 >= lo;
+                float mx = -INFINITY;
+                if (all_visible) {
 #pragma unroll
-            for (int c8 = 0; c8 < BN / 8; ++c8) {
-                float e[8];
+                    for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) e[i] = ex2_approx(s[c8 * 8 + i] - m_use);
-                uint32_t pk[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    pk[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
-                    // The denominator sums the bf16 weights the MMA actually uses.
-                    l_sum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    for (int c = 0; c < BN; ++c) {
+                        const int k = key0 + c;
+                        if (k > pos || k < lo) s[c] = -INFINITY;
+                        mx = fmaxf(mx, s[c]);
+                    }
                 }
-                const uint32_t addr = sP + (c8 >> 3) * HALF + row * 128 +
-                                      ((((c8 & 7) ^ (row & 7))) << 4);
-                st_shared_v4(addr, pk[0], pk[1], pk[2], pk[3]);
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                if (j == 0) {
+                    m_ref = m_new;  // O holds nothing of this item yet
+                } else {
+                    const bool need = m_new > m_ref + 8.f;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // Rescale O: wait until P V(t-1) has landed in it.
+                        if (!wait_warp(bar(B_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
+                                       abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
+#pragma unroll 1
+                        for (int c = 0; c < HD / 32; ++c) {
+                            float o[32];
+                            tmem_ld_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= f;
+                            tmem_st_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
+                        }
+                        l_sum *= f;
+                        if (need) m_ref = m_new;
+                    }
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+
+                // P = 2^(s * scale_log2 - m) as bf16 into the low 64 columns of the S
+                // buffer; the denominator sums the bf16 weights the MMA actually uses.
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float e0 = ex2_approx(fmaf(s[c * 64 + 2 * i], sl2, -m_use));
+                        const float e1 = ex2_approx(fmaf(s[c * 64 + 2 * i + 1], sl2, -m_use));
+                        pk[i] = pack_bf16x2(e0, e1);
+                        l_sum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    }
+                    tmem_st_32x32b_x32_u(tmem + scol + c * 32, pk);
+                }
+                // Keys of the sequence's last, partly filled 16-key piece that lie past sk
+                // are stale cache rows: zero them in the V tile so 0 * V stays 0.
+                if (((it.sk - 1) / BN) == it.kt0 + j && (it.sk & 15) != 0) {
+                    const int st = t % NSV;
+                    if (!wait_warp(bar(B_VFULL + st), (t / NSV) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int r0 = it.sk - key0;  // first stale row in the tile
+                    const int nrows = 16 - (it.sk & 15);
+                    const uint32_t vb = sV + st * L::TILE;
+                    for (int i2 = row; i2 < nrows * 8 * NHALF; i2 += 128) {
+                        const int r = r0 + i2 / (8 * NHALF);
+                        const int rest = i2 % (8 * NHALF);
+                        st_shared_v4(vb + (rest >> 3) * HALF + r * 128 + ((rest & 7) << 4), 0u, 0u,
+                                     0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_PFULL + (t & 1)));
             }
-            // Keys of the sequence's last, partly filled 16-key piece that lie past sk
-            // are stale cache rows: zero them in the V tile so 0 * V stays 0.
-            if (((sk - 1) / BN) == kt0 + j && (sk & 15) != 0) {
-                const int st = j % NSV;
-                if (!wait_warp(bar(B_VFULL + st), (j / NSV) & 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const int r0 = sk - key0;               // first stale row in the tile
-                const int nrows = 16 - (sk & 15);
-                const uint32_t vb = sV + st * L::TILE;
-                for (int idx = row; idx < nrows * 8 * NHALF; idx += 128) {
-                    const int r = r0 + idx / (8 * NHALF);
-                    const int rest = idx % (8 * NHALF);
-                    const uint32_t addr = vb + (rest >> 3) * HALF + r * 128 + ((rest & 7) << 4);
-                    st_shared_v4(addr, 0u, 0u, 0u, 0u);
-                }
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16 rows ----
+            // P V of the item's last tile (global t - 1); its completion implies all
+            // earlier ones.
+            if (!wait_warp(bar(B_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL));
-        }
-        // ---- epilogue: O / l -> bf16 rows ----
-        if (ok && wait_warp(bar(B_ODONE), (n_tiles - 1) & 1, abort_flag, p.err)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-            __nv_bfloat16 *dst = p.out +
-                                 (static_cast<int64_t>(q_start + q0 + tok) * p.num_heads +
-                                  kvh * G + g) * HD;
+            __nv_bfloat16 *dst =
+                p.out + (static_cast<int64_t>(it.q_start + it.q0 + tok) * p.num_heads +
+                         it.kvh * G + g) * HD;
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 float o[32];
@@ -498,16 +563,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            tc_fence_before();
         }
-        tc_fence_before();
     }
 
     // ---- teardown: everyone done, then free tensor memory ----
     __syncthreads();
     if (*abort_flag) {
-        // Drain whatever this CTA still has in flight before its shared and tensor memory
-        // go away: outstanding tensor-core work (one commit after the last issue) and TMA
-        // loads (their full barriers), each wait bounded.
+        // Bounded drain: let tensor-core work and TMA loads still in flight land before
+        // this CTA's shared and tensor memory are released.
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 2000000ull) {
         }
@@ -551,6 +615,19 @@ bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uin
     return r == CUDA_SUCCESS;
 }
 
+int sm_count() {
+    static std::atomic<int> counts[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        counts[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <int HD>
 cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cudaStream_t stream) {
     using L = Layout<HD>;
@@ -568,8 +645,8 @@ cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cuda
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    const int q_tiles = (a.max_seqlen_q + kp.tok_per_tile - 1) / kp.tok_per_tile;
-    dim3 grid(q_tiles, a.num_kv_heads, a.num_seqs);
+    const int sms = sm_count();
+    const int grid = kp.n_items < sms ? kp.n_items : sms;
     kern<<<grid, kThreads, L::SMEM, stream>>>(kp);
     return cudaGetLastError();
 }
@@ -600,6 +677,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.num_kv_heads = a.num_kv_heads;
     kp.group = a.num_heads / a.num_kv_heads;
     kp.tok_per_tile = BM / kp.group;
+    kp.q_tiles = (a.max_seqlen_q + kp.tok_per_tile - 1) / kp.tok_per_tile;
+    const int64_t n_items = static_cast<int64_t>(kp.q_tiles) * a.num_kv_heads * a.num_seqs;
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kp.n_items = static_cast<int>(n_items);
     kp.window = a.sliding_window;
     kp.scale_log2 = a.scale * kLog2e;
     kp.err = a.err;

@@ -103,6 +103,8 @@ def test_prefill_argument_checks(lib):
     assert _prefill(lib, cuq=None) == INVALID
     assert _prefill(lib, slot=FAKE) == INVALID
     assert _prefill(lib, out=MISALIGNED) == INVALID
+    assert _prefill(lib, scale=0.0) == INVALID
+    assert _prefill(lib, scale=-0.1) == INVALID
 
 
 def test_decode_split_plan_is_consistent(lib):
