@@ -32,4 +32,4 @@ from ._lib import (  # noqa: F401
     status_string,
     version,
 )
-from .build import build  # noqa: F401
+from .builder import build  # noqa: F401

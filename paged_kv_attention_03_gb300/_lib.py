@@ -13,7 +13,7 @@ import threading
 
 import torch
 
-from . import build as _build
+from . import builder as _build
 
 _lock = threading.Lock()
 _lib = None
