@@ -10,26 +10,27 @@
 //
 // GB300 design (the page's Triton kernel uses 32x32 or 64x64 tiles sized for ~48 KB of
 // shared memory and reads contiguous K/V):
-//  * Work item = (128-row query tile, kv head, sequence).  The 128 MMA rows pack the G
-//    query heads of one kv head for T = floor(128 / G) consecutive tokens (row m =
-//    token m / G, head m % G), so one K/V tile feeds all heads of the group.
-//  * Persistent CTAs, one per SM, walk the items round-robin, longest query tiles
-//    first; the load / MMA / softmax pipelines run on across item boundaries (Q is
-//    double-buffered, every ring barrier counts tiles globally).
+//  * Query tile = 128 MMA rows packing the G query heads of one kv head for
+//    T = floor(128 / G) consecutive tokens (row m = token m / G, head m % G).  A work
+//    item is two consecutive query tiles (2T tokens) of one (sequence, kv head), so every
+//    K/V tile fetched feeds 256 rows: half the K/V bytes per FLOP of one tile.
+//  * Persistent CTAs, one per SM, walk the items round-robin, longest first; the next
+//    item's Q is prefetched into L2 while the current one runs.
 //  * K/V come straight from the paged cache: the TMA producers walk block_table and
 //    fetch each 16-key piece of a page as one 3-D box {64 dims, 1 kv head, 16 rows}
 //    with 128-byte swizzle; pieces past the sequence come from an out-of-range
 //    coordinate, which the TMA unit fills with zeros.
-//  * S = Q K^T (M=128, N=128 keys, K=head_dim) runs as tcgen05.mma kind::f16 with both
-//    operands in shared memory and the fp32 accumulator in tensor memory (two S buffers
-//    of 128 columns).  The softmax writes P as bf16 back into the first 64 columns of
-//    the same buffer, and O += P V (M=128, N=head_dim, K=128 keys) takes P straight
-//    from tensor memory, V from shared memory (N-major), O in 128 columns.
-//  * Warp roles: warp 0 loads Q and K, warp 6 loads V, warp 1 issues the MMAs (one
-//    thread), warps 2-5 own one accumulator row each (thread = TMEM lane): mask, online
-//    softmax in base 2 with the scale folded into the exponent, lazy O rescale (only
-//    when the running max grows by more than 2^8, so the softmax rarely waits for the
-//    previous P V), and the epilogue.
+//  * Tensor memory (512 columns): S0, S1 (one 128x128 fp32 logit tile per query tile)
+//    and O0, O1.  S_i = Q_i K^T runs as tcgen05.mma kind::f16 with both operands in
+//    shared memory; softmax warpgroup i writes P_i as bf16 over the first 64 columns of
+//    S_i, and O_i += P_i V takes P_i from tensor memory, V (N-major) from shared memory.
+//  * One thread issues the MMAs in the order ... P0 V(t-1), S0(t), P1 V(t-1), S1(t) ...,
+//    so each softmax warpgroup works on its tile while the tensor core runs the other
+//    tile's products (ping-pong).
+//  * Warp roles: 0 loads Q and K, 10 loads V, 1 issues MMAs, 2-5 and 6-9 are the two
+//    softmax warpgroups (thread = TMEM lane = accumulator row): mask, online softmax in
+//    base 2 with the scale folded into the exponent, lazy O rescale (only when the
+//    running max grows by more than 2^8), epilogue.
 //  * Every mbarrier wait is bounded: on timeout the CTA raises an error bit, drains,
 //    frees its tensor memory and returns.
 #include <cuda.h>
@@ -52,14 +53,17 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128;                  // MMA rows per work item
+constexpr int BM = 128;                  // MMA rows per query tile
 constexpr int BN = 128;                  // keys per KV tile
 constexpr uint32_t HALF = 128u * 128u;   // [128 rows][64 bf16] = 16 KB (one swizzle span)
 constexpr int NSK = 3;                   // K stages
 constexpr int NSV = 2;                   // V stages
-constexpr int kThreads = 224;            // 7 warps
+constexpr int kWarpQK = 0, kWarpMma = 1, kWarpV = 10;
+constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// Tensor-memory columns: S_i at 128 * i, O_i at 256 + 128 * i.
+__host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
+__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * static_cast<uint32_t>(i); }
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 struct PrefillKernelParams {
@@ -74,8 +78,8 @@ struct PrefillKernelParams {
     int max_num_blocks;
     int num_seqs;
     int max_seqlen_q;
-    int q_tiles;  // ceil(max_seqlen_q / tok_per_tile)
-    int n_items;  // q_tiles * num_kv_heads * num_seqs
+    int q_items;  // ceil(max_seqlen_q / (2 * tok_per_tile))
+    int n_items;  // q_items * num_kv_heads * num_seqs
     int64_t seq_cap;  // max_num_blocks * block_size, capped by max_seqlen_k
     int64_t num_blocks;
     int log2_bs;
@@ -91,14 +95,14 @@ struct PrefillKernelParams {
 // Barrier indices.
 enum : int {
     B_QFULL = 0,
-    B_QEMPTY = B_QFULL + 2,
-    B_KFULL = B_QEMPTY + 2,
+    B_QEMPTY = 1,
+    B_KFULL = 2,
     B_KEMPTY = B_KFULL + NSK,
     B_VFULL = B_KEMPTY + NSK,
     B_VEMPTY = B_VFULL + NSV,
-    B_SFULL = B_VEMPTY + NSV,
-    B_PFULL = B_SFULL + 2,  // one per S buffer (tile parity)
-    B_ODONE = B_PFULL + 2,  // one per S buffer: keeps every waiter within one phase
+    B_SFULL = B_VEMPTY + NSV,  // [2]: one per query tile
+    B_PFULL = B_SFULL + 2,     // [2]
+    B_ODONE = B_PFULL + 2,     // [2]
     NBARS = B_ODONE + 2
 };
 
@@ -106,7 +110,7 @@ template <int HD>
 struct Layout {
     static constexpr int NHALF = HD / 64;
     static constexpr uint32_t TILE = NHALF * HALF;  // one [128][HD] bf16 tile
-    static constexpr uint32_t OFF_Q = 0;             // two Q buffers
+    static constexpr uint32_t OFF_Q = 0;             // Q0, Q1
     static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
@@ -119,17 +123,19 @@ struct Layout {
 // Geometry of one work item; every role derives it identically.
 struct Item {
     bool valid;
-    int seq, kvh, q0, rows_tok, q_start, sq, sk, kt0, n_tiles;
+    bool has1;  // the second query tile has rows
+    int seq, kvh, q0, rows0, rows1, q_start, sq, sk, kt0, n_tiles;
 };
 
 __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, bool report) {
     Item it;
-    const int per_qt = p.num_kv_heads * p.num_seqs;
-    const int qt = p.q_tiles - 1 - idx / per_qt;  // longest-running tiles first
-    const int rem = idx - (idx / per_qt) * per_qt;
+    const int per_q = p.num_kv_heads * p.num_seqs;
+    const int qi = p.q_items - 1 - idx / per_q;  // longest-running items first
+    const int rem = idx - (idx / per_q) * per_q;
     it.seq = rem / p.num_kv_heads;
     it.kvh = rem - it.seq * p.num_kv_heads;
     it.valid = false;
+    it.has1 = false;
     it.q_start = p.cu_q[it.seq];
     it.sq = p.cu_q[it.seq + 1] - it.q_start;
     int sk;
@@ -149,11 +155,14 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
         if (report) flag_error(p.err, kErrQueryLen);
         if (it.sq < 0 || it.sq > sk) return it;
     }
-    it.q0 = qt * p.tok_per_tile;
+    const int T = p.tok_per_tile;
+    it.q0 = qi * 2 * T;
     if (it.q0 >= it.sq) return it;
-    it.rows_tok = min(p.tok_per_tile, it.sq - it.q0);
+    it.rows0 = min(T, it.sq - it.q0);
+    it.rows1 = max(0, min(T, it.sq - it.q0 - T));
+    it.has1 = it.rows1 > 0;
     const int p_lo = sk - it.sq + it.q0;
-    const int p_hi = p_lo + it.rows_tok - 1;
+    const int p_hi = p_lo + it.rows0 + it.rows1 - 1;
     const int kmin = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
     it.kt0 = kmin / BN;
     it.n_tiles = p_hi / BN - it.kt0 + 1;
@@ -233,16 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.group;
+    const int T = p.tok_per_tile;
+    const uint32_t q_tile_bytes = static_cast<uint32_t>(G * T) * 128u * NHALF;
 
     // ---- set-up: barriers, tensor memory ----
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_QFULL + s), 1);
-            mbar_init(bar(B_QEMPTY + s), 1);
-            mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_PFULL + s), 4);
-            mbar_init(bar(B_ODONE + s), 1);
-        }
+        mbar_init(bar(B_QFULL), 1);
+        mbar_init(bar(B_QEMPTY), 1);
         for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
             mbar_init(bar(B_KEMPTY + s), 1);
@@ -251,11 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_VEMPTY + s), 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_SFULL + i), 1);
+            mbar_init(bar(B_PFULL + i), 4);
+            mbar_init(bar(B_ODONE + i), 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(base + L::OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
@@ -277,26 +288,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return (blk << p.log2_bs) | (k0 & bs_mask);
     };
+    // One K or V tile (128 keys) of item `it` into shared memory at dst.
+    auto load_kv = [&](const CUtensorMap *map, const Item &it, int key0, uint32_t dst,
+                       uint32_t full) {
+#pragma unroll 1
+        for (int u = 0; u < BN / 16; ++u) {
+            const int row = kv_row(it, key0 + u * 16);
+#pragma unroll
+            for (int h = 0; h < NHALF; ++h)
+                tma_load_3d(dst + h * HALF + u * 2048, map, h * 64, it.kvh, row, full);
+        }
+    };
 
-    if (warp == 0) {
+    if (warp == kWarpQK) {
         // ---------------- Q + K producer ----------------
         if (lane == 0) {
             prefetch_tmap(&p.tmap_q);
             prefetch_tmap(&p.tmap_k);
             uint32_t t = 0, ic = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item(p, idx, false);
-                if (!it.valid) continue;
-                const int qb = ic & 1;
-                if (ic >= 2 && !wait1(bar(B_QEMPTY + qb), ((ic >> 1) - 1) & 1, abort_flag, p.err))
-                    break;
-                mbar_arrive_expect_tx(bar(B_QFULL + qb),
-                                      static_cast<uint32_t>(G * p.tok_per_tile) * 128u * NHALF);
+            int idx = blockIdx.x;
+            Item it = get_item(p, idx, false);
+            while (ok && idx < p.n_items) {
+                if (!it.valid) {
+                    idx += gridDim.x;
+                    if (idx < p.n_items) it = get_item(p, idx, false);
+                    continue;
+                }
+                // Look ahead to the next valid item and pull its Q into L2.
+                int nidx = idx + gridDim.x;
+                Item nit;
+                nit.valid = false;
+                while (nidx < p.n_items) {
+                    nit = get_item(p, nidx, false);
+                    if (nit.valid) break;
+                    nidx += gridDim.x;
+                }
+                if (ic >= 1 && !wait1(bar(B_QEMPTY), (ic - 1) & 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
 #pragma unroll
-                for (int h = 0; h < NHALF; ++h)
-                    tma_load_3d(sQ + qb * L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
-                                it.q_start + it.q0, bar(B_QFULL + qb));
+                for (int h = 0; h < NHALF; ++h) {
+                    tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G, it.q_start + it.q0,
+                                bar(B_QFULL));
+                    if (it.has1)
+                        tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                    it.q_start + it.q0 + T, bar(B_QFULL));
+                }
+                if (nidx < p.n_items && nit.valid) {
+#pragma unroll
+                    for (int h = 0; h < NHALF; ++h) {
+                        tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G, nit.q_start + nit.q0);
+                        if (nit.has1)
+                            tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
+                                               nit.q_start + nit.q0 + T);
+                    }
+                }
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSK;
                     if (t >= NSK &&
@@ -304,22 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const int key0 = (it.kt0 + j) * BN;
                     mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
-                    const uint32_t dst = sK + st * L::TILE;
-#pragma unroll 1
-                    for (int u = 0; u < BN / 16; ++u) {
-                        const int row = kv_row(it, key0 + u * 16);
-#pragma unroll
-                        for (int h = 0; h < NHALF; ++h)
-                            tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_k, h * 64, it.kvh, row,
-                                        bar(B_KFULL + st));
-                    }
+                    load_kv(&p.tmap_k, it, (it.kt0 + j) * BN, sK + st * L::TILE, bar(B_KFULL + st));
                 }
                 ++ic;
+                idx = nidx;
+                it = nit;
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == kWarpV) {
         // ---------------- V producer (also reports per-sequence input errors) ----------------
         if (lane == 0) {
             prefetch_tmap(&p.tmap_v);
@@ -335,119 +374,141 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const int key0 = (it.kt0 + j) * BN;
                     mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
-                    const uint32_t dst = sV + st * L::TILE;
-#pragma unroll 1
-                    for (int u = 0; u < BN / 16; ++u) {
-                        const int row = kv_row(it, key0 + u * 16);
-#pragma unroll
-                        for (int h = 0; h < NHALF; ++h)
-                            tma_load_3d(dst + h * HALF + u * 2048, &p.tmap_v, h * 64, it.kvh, row,
-                                        bar(B_VFULL + st));
-                    }
+                    load_kv(&p.tmap_v, it, (it.kt0 + j) * BN, sV + st * L::TILE, bar(B_VFULL + st));
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ---------------- MMA issuer ----------------
-        // Order on the tensor pipe: S(t), P V(t-1), S(t+1), P V(t), ... across items.
+        // Order on the tensor pipe, across items: P0 V(g-1), S0(g), P1 V(g-1), S1(g).
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
-            uint32_t t = 0, ic = 0;
+            uint32_t g = 0;                  // global KV tile counter
+            uint32_t cnt[2] = {0, 0};        // tiles issued per query tile (S / P V)
+            uint32_t ic = 0;                 // items
             bool ok = true;
-            bool have_prev = false;
-            uint32_t prev_t = 0;
-            bool prev_first = false;
-            auto issue_pv = [&](uint32_t tt, bool first) -> bool {
-                const int st = tt % NSV;
-                if (!wait1(bar(B_PFULL + (tt & 1)), (tt >> 1) & 1, abort_flag, p.err)) return false;
-                if (!wait1(bar(B_VFULL + st), (tt / NSV) & 1, abort_flag, p.err)) return false;
+            // Pending P V of the previous KV tile: its V stage, whether it is the first tile
+            // of its item (overwrite O), and whether query tile 1 takes part.
+            bool have_prev = false, prev_first = false, prev_has1 = false;
+            uint32_t prev_g = 0;
+            auto issue_pv = [&](int i, uint32_t gv, bool first) -> bool {
+                const uint32_t c = cnt[i]++;
+                if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err)) return false;
+                if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err))
+                    return false;
                 tc_fence_after();
-                const uint32_t vbase = sV + st * L::TILE;
-                const uint32_t pcol = tmem + ((tt & 1) ? kColS1 : kColS0);
+                const uint32_t vbase = sV + (gv % NSV) * L::TILE;
 #pragma unroll
                 for (int k = 0; k < KSTEPS_O; ++k) {
                     const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
-                    mma_bf16_ts(tmem + kColO, pcol + k * 8, b, idesc_o,
+                    mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, b, idesc_o,
                                 (!first || k > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_ODONE + (tt & 1)));
-                mma_commit(bar(B_VEMPTY + st));
+                mma_commit(bar(B_ODONE + i));
+                return true;
+            };
+            auto issue_s = [&](int i, uint32_t gk) {
+                const uint32_t qbase = sQ + i * L::TILE;
+                const uint32_t kbase = sK + (gk % NSK) * L::TILE;
+#pragma unroll
+                for (int k = 0; k < KSTEPS_S; ++k) {
+                    const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
+                    mma_bf16_ss(tmem + col_s(i), a, b, idesc_s, k > 0);
+                }
+                mma_commit(bar(B_SFULL + i));
+            };
+            // Issue the P V products still pending from the previous KV tile.
+            auto flush = [&]() -> bool {
+                if (!have_prev) return true;
+                have_prev = false;
+                if (!issue_pv(0, prev_g, prev_first)) return false;
+                if (prev_has1 && !issue_pv(1, prev_g, prev_first)) return false;
+                mma_commit(bar(B_VEMPTY + prev_g % NSV));
                 return true;
             };
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
                 const Item it = get_item(p, idx, false);
                 if (!it.valid) continue;
-                const int qb = ic & 1;
-                if (!wait1(bar(B_QFULL + qb), (ic >> 1) & 1, abort_flag, p.err)) break;
-                const uint32_t qbase = sQ + qb * L::TILE;
-                for (int j = 0; j < it.n_tiles; ++j, ++t) {
-                    const int st = t % NSK;
-                    if (!wait1(bar(B_KFULL + st), (t / NSK) & 1, abort_flag, p.err)) {
+                // Finish the previous item before waiting for this item's Q, so its
+                // epilogue never waits on a Q load.
+                if (!flush()) break;
+                if (!wait1(bar(B_QFULL), ic & 1, abort_flag, p.err)) break;
+                for (int j = 0; j < it.n_tiles; ++j, ++g) {
+                    const int st = g % NSK;
+                    if (!wait1(bar(B_KFULL + st), (g / NSK) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbase = sK + st * L::TILE;
-                    const uint32_t scol = tmem + ((t & 1) ? kColS1 : kColS0);
-#pragma unroll
-                    for (int k = 0; k < KSTEPS_S; ++k) {
-                        const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
-                        const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                        mma_bf16_ss(scol, a, b, idesc_s, k > 0);
-                    }
-                    mma_commit(bar(B_SFULL + (t & 1)));
-                    mma_commit(bar(B_KEMPTY + st));
-                    if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY + qb));
-                    if (have_prev && !issue_pv(prev_t, prev_first)) {
+                    // query tile 0
+                    if (have_prev && !issue_pv(0, prev_g, prev_first)) {
                         ok = false;
                         break;
                     }
+                    issue_s(0, g);
+                    // query tile 1
+                    if (have_prev && prev_has1 && !issue_pv(1, prev_g, prev_first)) {
+                        ok = false;
+                        break;
+                    }
+                    if (have_prev) mma_commit(bar(B_VEMPTY + prev_g % NSV));
+                    if (it.has1) issue_s(1, g);
+                    mma_commit(bar(B_KEMPTY + st));
+                    if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY));
                     have_prev = true;
-                    prev_t = t;
+                    prev_g = g;
                     prev_first = j == 0;
+                    prev_has1 = it.has1;
                 }
                 ++ic;
             }
-            if (ok && have_prev) issue_pv(prev_t, prev_first);
+            if (ok) flush();
         }
     } else {
-        // ---------------- softmax / correction / epilogue (warps 2..5) ----------------
+        // ---------------- softmax warpgroups (warps 2..5: tile 0, 6..9: tile 1) ----------------
+        const int wg = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-        const int tok = row / G;
-        const int g = row - tok * G;
+        const uint32_t scol = tmem + t_lane + col_s(wg);
+        const uint32_t ocol = tmem + t_lane + col_o(wg);
+        const int tok = wg * T + row / G;  // token offset within the item
+        const int g = row - (row / G) * G;
+        const bool row_in_tile = row < G * T;
         const float sl2 = p.scale_log2;
         const int w = p.window;
-        uint32_t t = 0;
+        uint32_t gt = 0;   // global KV tile counter
+        uint32_t c = 0;    // tiles this warpgroup has processed
         bool ok = true;
         for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
             const Item it = get_item(p, idx, false);
             if (!it.valid) continue;
-            const bool valid = tok < it.rows_tok;
+            if (wg == 1 && !it.has1) {
+                gt += it.n_tiles;
+                continue;
+            }
+            const bool valid = row_in_tile && tok < it.rows0 + it.rows1;
             const int pos = it.sk - it.sq + it.q0 + tok;
             const int lo = w > 0 ? pos - w + 1 : INT_MIN;
             float m_ref = -INFINITY;  // reference max (base-2 units) the weights use
             float l_sum = 0.f;
-            for (int j = 0; j < it.n_tiles; ++j, ++t) {
-                const int sbuf = t & 1;
-                const uint32_t scol = t_lane + (sbuf ? kColS1 : kColS0);
-                if (!wait_warp(bar(B_SFULL + sbuf), (t >> 1) & 1, abort_flag, p.err)) {
+            for (int j = 0; j < it.n_tiles; ++j, ++gt, ++c) {
+                if (!wait_warp(bar(B_SFULL + wg), c & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float s[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int cc = 0; cc < BN / 32; ++cc) {
                     float v[32];
-                    tmem_ld_32x32b_x32(tmem + scol + c * 32, v);
+                    tmem_ld_32x32b_x32(scol + cc * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = v[i];
                 }
                 tmem_wait_ld();
 
@@ -456,13 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mx = -INFINITY;
                 if (all_visible) {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+                    for (int i = 0; i < BN; ++i) mx = fmaxf(mx, s[i]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        const int k = key0 + c;
-                        if (k > pos || k < lo) s[c] = -INFINITY;
-                        mx = fmaxf(mx, s[c]);
+                    for (int i = 0; i < BN; ++i) {
+                        const int k = key0 + i;
+                        if (k > pos || k < lo) s[i] = -INFINITY;
+                        mx = fmaxf(mx, s[i]);
                     }
                 }
                 const float m_new = fmaxf(m_ref, mx * sl2);
@@ -471,22 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     const bool need = m_new > m_ref + 8.f;
                     if (__any_sync(0xffffffffu, need)) {
-                        // Rescale O: wait until P V(t-1) has landed in it.
-                        if (!wait_warp(bar(B_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
-                                       abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                        // S(c) was issued after P V(c-1), so seeing it complete means O
+                        // already holds every earlier tile: rescale it in place.
                         const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
 #pragma unroll 1
-                        for (int c = 0; c < HD / 32; ++c) {
+                        for (int cc = 0; cc < HD / 32; ++cc) {
                             float o[32];
-                            tmem_ld_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
+                            tmem_ld_32x32b_x32(ocol + cc * 32, o);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] *= f;
-                            tmem_st_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
+                            tmem_st_32x32b_x32(ocol + cc * 32, o);
                         }
                         l_sum *= f;
                         if (need) m_ref = m_new;
@@ -494,25 +550,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
 
-                // P = 2^(s * scale_log2 - m) as bf16 into the low 64 columns of the S
-                // buffer; the denominator sums the bf16 weights the MMA actually uses.
+                // P = 2^(s * scale_log2 - m) as bf16 over the low 64 columns of S; the
+                // denominator sums the bf16 weights the MMA actually uses.
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2_approx(fmaf(s[c * 64 + 2 * i], sl2, -m_use));
-                        const float e1 = ex2_approx(fmaf(s[c * 64 + 2 * i + 1], sl2, -m_use));
+                        const float e0 = ex2_approx(fmaf(s[cc * 64 + 2 * i], sl2, -m_use));
+                        const float e1 = ex2_approx(fmaf(s[cc * 64 + 2 * i + 1], sl2, -m_use));
                         pk[i] = pack_bf16x2(e0, e1);
                         l_sum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
                     }
-                    tmem_st_32x32b_x32_u(tmem + scol + c * 32, pk);
+                    tmem_st_32x32b_x32_u(scol + cc * 32, pk);
                 }
                 // Keys of the sequence's last, partly filled 16-key piece that lie past sk
-                // are stale cache rows: zero them in the V tile so 0 * V stays 0.
-                if (((it.sk - 1) / BN) == it.kt0 + j && (it.sk & 15) != 0) {
-                    const int st = t % NSV;
-                    if (!wait_warp(bar(B_VFULL + st), (t / NSV) & 1, abort_flag, p.err)) {
+                // are stale cache rows: warpgroup 0 zeroes them in the V tile (before
+                // either P V of this tile is issued) so 0 * V stays 0.
+                if (wg == 0 && ((it.sk - 1) / BN) == it.kt0 + j && (it.sk & 15) != 0) {
+                    const int st = gt % NSV;
+                    if (!wait_warp(bar(B_VFULL + st), (gt / NSV) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
@@ -530,28 +587,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_PFULL + (t & 1)));
+                if (lane == 0) mbar_arrive(bar(B_PFULL + wg));
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> bf16 rows ----
-            // P V of the item's last tile (global t - 1); its completion implies all
-            // earlier ones.
-            if (!wait_warp(bar(B_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, p.err)) {
+            // ---- epilogue: O / l -> bf16 rows (P V of the item's last tile is number c-1) ----
+            if (!wait_warp(bar(B_ODONE + wg), (c - 1) & 1, abort_flag, p.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-            __nv_bfloat16 *dst =
-                p.out + (static_cast<int64_t>(it.q_start + it.q0 + tok) * p.num_heads +
-                         it.kvh * G + g) * HD;
+            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(it.q_start + it.q0 + tok) *
+                                              p.num_heads + it.kvh * G + g) * HD;
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int cc = 0; cc < HD / 32; ++cc) {
                 float o[32];
-                tmem_ld_32x32b_x32(tmem + t_lane + kColO + c * 32, o);
+                tmem_ld_32x32b_x32(ocol + cc * 32, o);
                 tmem_wait_ld();
                 if (valid) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         uint4 v;
@@ -577,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -677,8 +731,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.num_kv_heads = a.num_kv_heads;
     kp.group = a.num_heads / a.num_kv_heads;
     kp.tok_per_tile = BM / kp.group;
-    kp.q_tiles = (a.max_seqlen_q + kp.tok_per_tile - 1) / kp.tok_per_tile;
-    const int64_t n_items = static_cast<int64_t>(kp.q_tiles) * a.num_kv_heads * a.num_seqs;
+    const int item_tokens = 2 * kp.tok_per_tile;
+    kp.q_items = (a.max_seqlen_q + item_tokens - 1) / item_tokens;
+    const int64_t n_items = static_cast<int64_t>(kp.q_items) * a.num_kv_heads * a.num_seqs;
     if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
     kp.n_items = static_cast<int>(n_items);
     kp.window = a.sliding_window;
