@@ -36,6 +36,13 @@ from paged_kv_attention_03_gb300.inputs import WORKLOADS, make_case, split_mixed
 
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
+# DRAM bytes (read + write) of one launch on the default workloads, from the ncu
+# captures summarised in profiles/ (commands there); None once a kernel changes.
+NCU_TRAFFIC = {
+    "decode_split_kernel": 639.57e6 + 4.75e6,
+    "prefill_kernel": 286.52e6 + 106.75e6,
+}
+
 
 # ----------------------------------------------------------------- helpers ---
 
@@ -496,7 +503,11 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_split_kernel + combine)",
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"], "traffic": None,
+                     "peak_source": peaks["source"],
+                     "traffic": (NCU_TRAFFIC["decode_split_kernel"]
+                                 if args.workload == "batched_decode" else None),
+                     "traffic_kernel": "decode_split_kernel",
+                     "algorithmic_bytes": runner.work,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -526,10 +537,12 @@ def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):
     return {"metric": "varlen prefill TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s",
             "ms_per_step": round(statistics.mean(ms), 4), "flops_per_step": runner.work,
             "workload": "varlen_prefill: 16 prompts U[128,2048], 32/8 heads, D=128, bs=16",
-            "roofline": {"bound": "tensor", "kernel": "pa_varlen_prefill",
+            "roofline": {"bound": "tensor", "kernel": "pa_varlen_prefill (prefill_kernel)",
                          "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                         "peak_source": peaks["source"]}}
+                         "peak_source": peaks["source"],
+                         "traffic": NCU_TRAFFIC["prefill_kernel"],
+                         "algorithmic_flops": runner.work}}
 
 
 if __name__ == "__main__":

@@ -410,27 +410,41 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     }
     const float *ml = p.ws_ml + bh * p.num_splits * 2;
     const float *os = p.ws_o + bh * p.num_splits * D + lane * PER_LANE;
+    // Split s's (m, l) live in lane s % 32; one round trip for all of them.
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        const int s = s0 + lane;
+        const float m = s < nsplit ? ml[2 * s] : -INFINITY;
+        M = fmaxf(M, m);
+    }
+    M = warp_max(M);
     float wsum = 0.f;
     float acc[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const float w = ml[2 * s + 1] * ex2_approx(ml[2 * s] - M);
-        wsum += w;
-        const float *src = os + static_cast<int64_t>(s) * D;
-        if constexpr (PER_LANE == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
-        } else {
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        const int s = s0 + lane;
+        const float wl = s < nsplit ? ml[2 * s + 1] * ex2_approx(ml[2 * s] - M) : 0.f;
+        wsum += wl;
+        const int n = min(32, nsplit - s0);
+        // The partial rows of these splits, four loads in flight per lane.
+#pragma unroll 4
+        for (int k = 0; k < n; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            const float *src = os + static_cast<int64_t>(s0 + k) * D;
+            if constexpr (PER_LANE == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+                acc[2] += w * v.z;
+                acc[3] += w * v.w;
+            } else {
 #pragma unroll
-            for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
+                for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
+            }
         }
     }
+    wsum = warp_sum(wsum);
     const float inv = 1.f / wsum;
 #pragma unroll
     for (int i = 0; i < PER_LANE; i += 2)

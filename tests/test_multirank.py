@@ -1,0 +1,70 @@
+"""Host-side multi-rank logic of bench.py, on CPU with the gloo backend (world size 2).
+
+The path shards with no data exchange (each rank runs its own replica), so what is
+tested is the plumbing around it: rank discovery, distinct per-rank inputs, the
+max-over-ranks timing and the sum-over-ranks work count that make `value`.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_attention_03_gb300.inputs import make_case
+
+    r, local, ws = bench._dist()
+    assert (r, local, ws) == (rank, rank, world)
+    case = make_case("tiny_decode", seed=r)  # one replica per rank, own seed
+    t = bench._max_over_ranks(1.0 + r, ws, "cpu")
+    n = bench._sum_over_ranks(float(bench.decode_kv_bytes(case)), ws, "cpu")
+    bench._barrier(ws)
+    q.put((r, t, n, case.q.float().sum().item()))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_rank_timing_and_work_reduction():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, t0, n0, s0), (r1, t1, n1, s1) = res
+    assert t0 == t1 == 2.0  # max over ranks of 1.0 and 2.0
+    assert n0 == n1 and n0 > 0  # both ranks see the total work
+    assert s0 != s1  # distinct per-rank inputs
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny_decode", "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["value"] > 0 and rec["unit"] == "GB/s"
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
