@@ -514,18 +514,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 const int key0 = (it.kt0 + j) * BN;
                 const bool all_visible = key0 + BN - 1 <= pos && key0 >= lo;
-                float mx = -INFINITY;
-                if (all_visible) {
-#pragma unroll
-                    for (int i = 0; i < BN; ++i) mx = fmaxf(mx, s[i]);
-                } else {
+                // Row maximum as 8 independent 3-input max chains, then a tree (a single
+                // dependent chain of 128 maxima would cost ~4 cycles per element).
+                if (!all_visible) {
 #pragma unroll
                     for (int i = 0; i < BN; ++i) {
                         const int k = key0 + i;
                         if (k > pos || k < lo) s[i] = -INFINITY;
-                        mx = fmaxf(mx, s[i]);
                     }
                 }
+                static_assert(BN == 128, "the max tree covers 128 columns");
+                float mx8[8];  // mx8[a] = max over s[a + 8k], k = 0..15
+#pragma unroll
+                for (int a = 0; a < 8; ++a) mx8[a] = max3f(s[a], s[a + 8], s[a + 16]);
+#pragma unroll
+                for (int k = 3; k < 15; k += 2) {
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        mx8[a] = max3f(mx8[a], s[a + 8 * k], s[a + 8 * k + 8]);
+                }
+#pragma unroll
+                for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], s[a + 120]);
+                const float mx = fmaxf(fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5])),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 if (j == 0) {
                     m_ref = m_new;  // O holds nothing of this item yet
@@ -552,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // P = 2^(s * scale_log2 - m) as bf16 over the low 64 columns of S; the
                 // denominator sums the bf16 weights the MMA actually uses.
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
@@ -560,10 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float e0 = ex2_approx(fmaf(s[cc * 64 + 2 * i], sl2, -m_use));
                         const float e1 = ex2_approx(fmaf(s[cc * 64 + 2 * i + 1], sl2, -m_use));
                         pk[i] = pack_bf16x2(e0, e1);
-                        l_sum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                        ls[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
                     }
                     tmem_st_32x32b_x32_u(scol + cc * 32, pk);
                 }
+                l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // Keys of the sequence's last, partly filled 16-key piece that lie past sk
                 // are stale cache rows: warpgroup 0 zeroes them in the V tile (before
                 // either P V of this tile is issued) so 0 * V stays 0.
