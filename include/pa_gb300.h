@@ -76,6 +76,13 @@ const char *pa_status_string(pa_status status);
 const char *pa_version(void);
 
 /*
+ * CUDA error text behind the most recent PA_ERR_CUDA returned on the calling host
+ * thread ("no error" if there was none).  Static storage owned by the CUDA runtime;
+ * reading it clears nothing.
+ */
+const char *pa_last_cuda_error_string(void);
+
+/*
  * pa_store_kvcache - "MinivLLM API docs - Attention", section store_kvcache, and
  * "05 Attention Backends", Q&A 2 (slot -> block, offset).
  *

@@ -28,13 +28,16 @@ DEVERR_TIMEOUT = 0x20
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
-            "pa_read_device_error", "pa_decode_noalloc")
+            "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string")
 
 
 class PAError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)}")
+        msg = f"{what}: {status_string(status)}"
+        if status == PA_ERR_CUDA:
+            msg += f" ({last_cuda_error_string()})"
+        super().__init__(msg)
 
 
 def library_path() -> str:
@@ -59,6 +62,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
         lib.pa_version.restype = ctypes.c_char_p
+        lib.pa_last_cuda_error_string.argtypes = []
+        lib.pa_last_cuda_error_string.restype = ctypes.c_char_p
         lib.pa_store_kvcache.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, vp]
         lib.pa_store_kvcache.restype = ctypes.c_int
         lib.pa_decode_num_splits.argtypes = [i32] * 7
@@ -86,6 +91,11 @@ def status_string(status: int) -> str:
 
 def version() -> str:
     return load().pa_version().decode()
+
+
+def last_cuda_error_string() -> str:
+    """CUDA error text behind the most recent PA_ERR_CUDA on this thread."""
+    return load().pa_last_cuda_error_string().decode()
 
 
 def _check(status: int, what: str) -> None:

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "pa_gb300.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -68,7 +69,7 @@ extern "C" pa_status pa_decode_noalloc(void *out, const void *q, const void *key
     if (need > 0) {
         cudaError_t err = cudaSuccess;
         scratch = scratch_address(&err);
-        if (scratch == nullptr) return PA_ERR_CUDA;
+        if (scratch == nullptr) return pa::cuda_status(err != cudaSuccess ? err : cudaErrorUnknown);
     }
     // Nothing in the scratch has to start at zero: every split the combine reads is
     // written first by the same call.

@@ -10,6 +10,19 @@
 #include "pa_gb300.h"
 #include "pa_internal.h"
 
+namespace pa {
+// Last CUDA error behind a PA_ERR_CUDA, per host thread.
+static thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+pa_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    t_last_cuda_error = e;
+    return PA_ERR_CUDA;
+}
+
+const char *last_cuda_error_string() { return cudaGetErrorString(t_last_cuda_error); }
+}  // namespace pa
+
 namespace {
 
 // One error word per device: kernels OR PA_DEVERR_* bits into it.
@@ -40,7 +53,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 
-pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+pa_status from_cuda(cudaError_t e) { return pa::cuda_status(e); }
 
 // Store-argument checks shared by the three entry points.
 pa_status check_store(const void *key, const void *value, const void *k_cache,
@@ -89,6 +102,8 @@ const char *pa_status_string(pa_status status) {
 }
 
 const char *pa_version(void) { return "pa_gb300 0.1 sm_103a"; }
+
+const char *pa_last_cuda_error_string(void) { return pa::last_cuda_error_string(); }
 
 pa_status pa_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
                            const int32_t *slot_mapping, int64_t num_tokens,
@@ -245,15 +260,18 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
 
 pa_status pa_read_device_error(void *stream, uint32_t *flags, int clear) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return from_cuda(e);
     unsigned *word = device_error_word();
     if (word == nullptr) return PA_ERR_CUDA;
     unsigned host = 0;
-    if (cudaMemcpy(&host, word, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
-        return PA_ERR_CUDA;
+    e = cudaMemcpy(&host, word, sizeof host, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
     if (clear && host != 0) {
-        if (cudaMemset(word, 0, sizeof host) != cudaSuccess) return PA_ERR_CUDA;
-        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+        e = cudaMemset(word, 0, sizeof host);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return from_cuda(e);
     }
     if (flags) *flags = host;
     return host == 0 ? PA_OK : PA_ERR_DEVICE_CHECK;

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pa_gb300.h"
+
 namespace pa {
 
 // ------------------------------------------------------------------ store ---
@@ -82,5 +84,8 @@ struct PrefillArgs {
     unsigned *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Map a CUDA error to a pa_status, remembering it for pa_last_cuda_error_string().
+pa_status cuda_status(cudaError_t e);
 
 }  // namespace pa

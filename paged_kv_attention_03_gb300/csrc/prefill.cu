@@ -502,15 +502,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float s[BN];
+                float sc[BN / 32][32];
 #pragma unroll
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    float v[32];
-                    tmem_ld_32x32b_x32(scol + cc * 32, v);
+                for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_32x32b_x32(scol + cc * 32, sc[cc]);
+                // The waits name the loaded registers, so no use of them moves above.
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[cc * 32 + i] = v[i];
-                }
-                tmem_wait_ld();
+                for (int cc = 0; cc < BN / 32; ++cc) tmem_wait_ld_regs(sc[cc]);
+                float *s = &sc[0][0];
 
                 const int key0 = (it.kt0 + j) * BN;
                 const bool all_visible = key0 + BN - 1 <= pos && key0 >= lo;
@@ -550,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int cc = 0; cc < HD / 32; ++cc) {
                             float o[32];
                             tmem_ld_32x32b_x32(ocol + cc * 32, o);
-                            tmem_wait_ld();
+                            tmem_wait_ld_regs(o);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] *= f;
                             tmem_st_32x32b_x32(ocol + cc * 32, o);
@@ -616,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < HD / 32; ++cc) {
                 float o[32];
                 tmem_ld_32x32b_x32(ocol + cc * 32, o);
-                tmem_wait_ld();
+                tmem_wait_ld_regs(o);
                 if (valid) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
 #pragma unroll

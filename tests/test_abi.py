@@ -129,3 +129,8 @@ def test_read_device_error_without_gpu_reports_cuda_error(lib):
         pytest.skip("only meaningful on a machine without a GPU")
     flags = ctypes.c_uint32(0)
     assert lib.pa_read_device_error(None, ctypes.byref(flags), 0) == pa.PA_ERR_CUDA
+    # The CUDA error behind that status is kept for the calling thread.
+    text = lib.pa_last_cuda_error_string().decode()
+    assert text and text != "no error"
+    with pytest.raises(pa.PAError, match=r"PA_ERR_CUDA \(.+\)"):
+        raise pa.PAError(pa.PA_ERR_CUDA, "probe")
