@@ -176,7 +176,7 @@ def prefill_flops(case, seqs=None):
 # ------------------------------------------------------------------ runners ---
 
 class DecodeRunner:
-    """One step: fused store of the new tokens + split-K decode (+ combine)."""
+    """One step: split-K decode with the store of the new tokens fused in (+ combine)."""
 
     def __init__(self, case, device, seqs=None):
         import paged_kv_attention_03_gb300 as pa
@@ -202,7 +202,8 @@ class DecodeRunner:
         need = pa.pa_decode_workspace_size(len(self.seqs), w.num_heads, w.num_kv_heads,
                                            w.head_dim, self.max_len, self.window, 0)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-        self.launches = 2 + (1 if self.splits > 1 else 0)
+        # The store of the new tokens runs inside the split kernel.
+        self.launches = 1 + (1 if self.splits > 1 else 0)
         self.work = decode_kv_bytes(case, self.seqs)
 
     def step(self):
@@ -238,7 +239,7 @@ class DecodeRunner:
 
 
 class PrefillRunner:
-    """One step: fused store of the prompt tokens + varlen causal prefill."""
+    """One step: store of the prompt tokens + varlen causal prefill (one call, two launches)."""
 
     def __init__(self, case, device):
         import paged_kv_attention_03_gb300 as pa
@@ -252,7 +253,7 @@ class PrefillRunner:
         self.bt = t(case.block_table)
         self.slots = t(case.slot_mapping)
         self.out = torch.empty_like(case.q)
-        self.launches = 2
+        self.launches = 2  # the store of the prompt tokens, then the prefill
         self.work = prefill_flops(case)
 
     def step(self):

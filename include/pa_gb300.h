@@ -68,6 +68,8 @@ typedef enum pa_status {
 #define PA_DEVERR_QUERY_LEN 0x8u   /* prefill: query_len > seq_len, or > max_seqlen_q */
 #define PA_DEVERR_SEQLENS_K 0x10u  /* prefill: cu_seqlens_k differences disagree with seq_lens */
 #define PA_DEVERR_TIMEOUT 0x20u    /* a pipeline wait gave up (internal error; output undefined) */
+#define PA_DEVERR_SLOT_MISMATCH 0x40u /* fused store: slot_mapping[t] >= 0 is not the cache row
+                                         of token t's own position (row still written) */
 
 /* Human-readable name of a status code (static storage). */
 const char *pa_status_string(pa_status status);
@@ -132,9 +134,14 @@ size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int 
  *   out           [batch, num_heads, head_dim] bf16, device (written)
  *   q             [batch, num_heads, head_dim] bf16, device, 16-byte aligned
  *   key, value, slot_mapping   optional (all NULL or all set): [batch, num_kv_heads,
- *                 head_dim] bf16 and [batch] int32.  When set, the call first stores
- *                 them into the cache exactly as pa_store_kvcache (same stream), so
- *                 the new token is visible to the attention that follows.
+ *                 head_dim] bf16 and [batch] int32, the new token of each sequence.
+ *                 When set, the same launch stores them into the cache as
+ *                 pa_store_kvcache would (slot < 0: skipped) before reading it: each
+ *                 block that reads key L - 1 writes that row first.  This requires
+ *                 slot_mapping[b] to be the cache row of position L - 1 of sequence b
+ *                 (or negative), as it is when derived from block_table; another slot
+ *                 is still written but raises PA_DEVERR_SLOT_MISMATCH, and the
+ *                 attention then reads whatever the row of L - 1 holds.
  *   k_cache, v_cache  the paged cache (written only by that optional store)
  *   block_table   [batch, max_num_blocks] int32, device
  *   seq_lens      [batch] int32, device

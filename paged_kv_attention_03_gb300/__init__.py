@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     DEVERR_SEQLENS_K,
     DEVERR_SLOT_RANGE,
     DEVERR_TIMEOUT,
+    DEVERR_SLOT_MISMATCH,
     EXPORTED,
     PA_ERR_CUDA,
     PA_ERR_DEVICE_CHECK,

@@ -25,6 +25,7 @@ DEVERR_SEQ_RANGE = 0x4
 DEVERR_QUERY_LEN = 0x8
 DEVERR_SEQLENS_K = 0x10
 DEVERR_TIMEOUT = 0x20
+DEVERR_SLOT_MISMATCH = 0x40
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",

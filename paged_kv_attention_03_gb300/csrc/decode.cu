@@ -56,6 +56,12 @@ struct DecodeKernelParams {
     int num_splits;
     float *ws_o;   // [batch, num_heads, num_splits, D] normalised partial outputs
     float *ws_ml;  // [batch, num_heads, num_splits, 2] (running max in log2 units, sum)
+    // Fused store of the new token of each sequence (null when not fused).
+    const __nv_bfloat16 *key;    // [batch, num_kv_heads, D]
+    const __nv_bfloat16 *value;
+    const int32_t *slot_mapping;  // [batch]
+    __nv_bfloat16 *kc_w;          // the caches, writable
+    __nv_bfloat16 *vc_w;
     unsigned *err;
 };
 
@@ -110,6 +116,41 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
     const int hi = min(sr.L, sr.base + (split + 1) * p.chunk);
     const int h0 = kvh * p.group + ht * 16;
     const int rows_valid = min(16, p.group - ht * 16);
+
+    // Fused store: a block that reads key L - 1 first writes this kv head's new token
+    // (its row of the cache) itself, so no other launch has to run before it.  Every
+    // such block writes the same bytes.  A sequence with no keys still gets its row
+    // written, by split 0 of head tile 0.
+    if (p.slot_mapping != nullptr &&
+        ((lo < hi && hi == sr.L) || (sr.L == 0 && split == 0 && ht == 0))) {
+        const int slot = p.slot_mapping[b];
+        const int64_t num_slots = p.num_blocks << p.log2_bs;
+        if (slot >= 0 && slot < num_slots) {
+            if (threadIdx.x < 2 * CPR) {
+                const int which = threadIdx.x / CPR;
+                const int c = threadIdx.x - which * CPR;
+                const int64_t src_row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
+                const int64_t dst_row = static_cast<int64_t>(slot) * p.num_kv_heads + kvh;
+                const uint4 v = reinterpret_cast<const uint4 *>((which ? p.value : p.key) +
+                                                                src_row * D)[c];
+                reinterpret_cast<uint4 *>((which ? p.vc_w : p.kc_w) + dst_row * D)[c] = v;
+            }
+            if (threadIdx.x == 0 && sr.L > 0 && ht == 0) {
+                // The attention reads key L - 1 through block_table: the slot must be there.
+                const int pos = sr.L - 1;
+                const int blk = p.block_table[static_cast<int64_t>(b) * p.max_num_blocks +
+                                              (pos >> p.log2_bs)];
+                const int64_t want =
+                    (static_cast<int64_t>(blk) << p.log2_bs) | (pos & ((1 << p.log2_bs) - 1));
+                if (want != slot) flag_error(p.err, kErrSlotMismatch);
+            }
+            if (threadIdx.x == 0 && sr.L == 0) flag_error(p.err, kErrSlotMismatch);
+        } else if (slot >= num_slots && threadIdx.x == 0) {
+            flag_error(p.err, kErrSlotRange);
+        }
+        // The block's own loads of the row (cp.async, after this barrier) see the write.
+        __syncthreads();
+    }
 
     if (lo >= hi) {
         // Empty split.  A sequence with no keys at all gets a zero row; with several
@@ -558,6 +599,11 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
         kp.ws_o = nullptr;
         kp.ws_ml = nullptr;
     }
+    kp.key = static_cast<const __nv_bfloat16 *>(a.key);
+    kp.value = static_cast<const __nv_bfloat16 *>(a.value);
+    kp.slot_mapping = a.slot_mapping;
+    kp.kc_w = static_cast<__nv_bfloat16 *>(a.k_cache_w);
+    kp.vc_w = static_cast<__nv_bfloat16 *>(a.v_cache_w);
     kp.err = a.err;
     switch (a.head_dim) {
         case 64: return launch_decode_d<64>(kp, plan, a.batch, stream);

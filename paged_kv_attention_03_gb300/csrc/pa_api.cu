@@ -170,9 +170,6 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
         const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, batch,
                                          num_blocks, block_size, num_kv_heads, head_dim);
         if (st != PA_OK) return st;
-        const pa_status rs = run_store(key, value, k_cache, v_cache, slot_mapping, batch,
-                                       num_blocks, block_size, num_kv_heads, head_dim, s);
-        if (rs != PA_OK) return rs;
     }
     pa::DecodeArgs a;
     a.out = out;
@@ -192,6 +189,12 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
     a.sliding_window = sliding_window;
     a.scale = scale;
     a.workspace = workspace;
+    // The new tokens are stored by the decode launch itself.
+    a.key = has_new ? key : nullptr;
+    a.value = has_new ? value : nullptr;
+    a.slot_mapping = has_new ? slot_mapping : nullptr;
+    a.k_cache_w = k_cache;
+    a.v_cache_w = v_cache;
     a.err = device_error_word();
     return from_cuda(pa::launch_decode(a, plan, s));
 }

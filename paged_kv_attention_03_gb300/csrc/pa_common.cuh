@@ -14,6 +14,7 @@ constexpr unsigned kErrBlockRange = 0x2u;
 constexpr unsigned kErrSeqRange = 0x4u;
 constexpr unsigned kErrQueryLen = 0x8u;
 constexpr unsigned kErrSeqlensK = 0x10u;
+constexpr unsigned kErrSlotMismatch = 0x40u;
 
 __device__ __forceinline__ void flag_error(unsigned *err, unsigned bit) {
     if (err != nullptr) atomicOr(err, bit);

@@ -55,6 +55,12 @@ struct DecodeArgs {
     int sliding_window;
     float scale;
     void *workspace;
+    // Fused store of each sequence's new token (all null when not fused).
+    const void *key;               // [batch, num_kv_heads, head_dim]
+    const void *value;
+    const int32_t *slot_mapping;   // [batch]
+    void *k_cache_w;               // the caches, writable
+    void *v_cache_w;
     unsigned *err;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);

@@ -43,6 +43,7 @@ def _full_check(case, dev, num_splits=0, window=None):
     out = _decode_case(case, dev, num_splits=num_splits, window=window)
     assert pa.pa_read_device_error(device=dev) == 0
     np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
     return assert_parity(out, ref, f"{case.workload.name} splits={num_splits}")
 
 

@@ -44,6 +44,7 @@ def _full_check(case, dev, window=None, **kw):
     flags = pa.pa_read_device_error(device=dev)
     assert flags == 0, f"device error bits {flags:#x}"
     np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
     return assert_parity(out, ref, case.workload.name)
 
 
