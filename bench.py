@@ -270,6 +270,48 @@ class PrefillRunner:
                                   c.workload.sliding_window, out=self.out)
 
 
+class MixedRunner:
+    """The mixed-window workload (chunked prefill + decodes, window 4096) two ways:
+    `single` = one pa_varlen_prefill call over the whole packed batch (store + prefill);
+    `split` = pa_varlen_prefill on the chunks, then pa_decode on the decode rows."""
+
+    def __init__(self, case, device):
+        import paged_kv_attention_03_gb300 as pa
+
+        self.pa = pa
+        self.case = case
+        pre, dec = split_mixed(case)
+        self.full = PrefillRunner(case, device)
+        t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=device)
+        cu = case.cu_seqlens_q
+        rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in pre])
+        r = torch.as_tensor(rows, dtype=torch.long, device=device)
+        self.pq, self.pkey, self.pval = case.q[r].contiguous(), case.key[r].contiguous(), \
+            case.value[r].contiguous()
+        ql = case.query_lens[pre]
+        sub_cu = np.zeros(len(pre) + 1, np.int32)
+        sub_cu[1:] = np.cumsum(ql)
+        self.pcu, self.psl = t(sub_cu), t(case.seq_lens[pre])
+        self.pbt, self.pslots = t(case.block_table[pre]), t(case.slot_mapping[rows])
+        self.pmax_q, self.pmax_k = int(ql.max()), int(case.seq_lens[pre].max())
+        self.pout = torch.empty_like(self.pq)
+        self.dec = DecodeRunner(case, device, dec)
+        self.chunk_flops = prefill_flops(case, pre)
+        self.decode_bytes = decode_kv_bytes(case, dec)
+        self.n_chunks, self.n_decodes = len(pre), len(dec)
+
+    def single(self):
+        self.full.step()
+
+    def split(self):
+        w = self.case.workload
+        self.pa.pa_varlen_prefill(self.pq, self.case.k_cache, self.case.v_cache, self.pcu,
+                                  self.psl, self.pbt, self.pmax_q, self.pmax_k, w.final_scale,
+                                  w.sliding_window, key=self.pkey, value=self.pval,
+                                  slot_mapping=self.pslots, out=self.pout)
+        self.dec.step()
+
+
 def _time_steps(fn, steps, warmup, flush, stream):
     """Per-step device time (ms) with CUDA events on `stream`, L2 flushed (untimed) before
     each step."""
@@ -394,6 +436,7 @@ def main():
                     choices=["batched_decode", "long_decode", "tiny_decode", "mixed_window"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
                     help="decode: the decode step only; prefill: the prefill step only "
                          "(profiling runs); both: the full JSON line")
@@ -480,6 +523,9 @@ def main():
     prefill = None
     if not args.no_prefill:
         prefill = _prefill_leg(pa, dev, rank, peaks, flush, stream, args)
+    mixed = None
+    if not args.no_mixed:
+        mixed = _mixed_leg(pa, dev, rank, peaks, flush, stream, args)
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and args.gpus == 1:
@@ -517,7 +563,29 @@ def main():
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if mixed is not None:
+        line["mixed"] = mixed
     print(json.dumps(line), flush=True)
+
+
+def _mixed_leg(pa, dev, rank, peaks, flush, stream, args):
+    """Step time of the mixed-window workload, one call and two calls, against the step's
+    roofline time: decode bytes / HBM peak + chunk FLOPs / bf16 peak."""
+    case = make_case(WORKLOADS["mixed_window"], seed=200 + rank, device=dev)
+    runner = MixedRunner(case, dev)
+    steps = max(20, args.steps // 10)
+    single = statistics.mean(_time_steps(runner.single, steps, 3, flush, stream))
+    split = statistics.mean(_time_steps(runner.split, steps, 3, flush, stream))
+    roof_ms = 1e3 * (runner.decode_bytes / (peaks["hbm_gbs"] * 1e9) +
+                     runner.chunk_flops / (peaks["bf16_tflops"] * 1e12))
+    return {"workload": f"mixed_window: {runner.n_chunks} chunks of 512 + "
+                        f"{runner.n_decodes} decodes, ctx U[1024,8192], window 4096",
+            "chunk_flops": runner.chunk_flops, "decode_bytes": runner.decode_bytes,
+            "roofline_ms": round(roof_ms, 4),
+            "single_call": {"ms_per_step": round(single, 4), "launches": 2,
+                            "frac_of_roofline": round(roof_ms / single, 4)},
+            "two_calls": {"ms_per_step": round(split, 4), "launches": 2 + runner.dec.launches,
+                          "frac_of_roofline": round(roof_ms / split, 4)}}
 
 
 def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) flush();
         }
-    } else {
+    } else if (warp >= 2 && warp < 10) {
         // ---------------- softmax warpgroups (warps 2..5: tile 0, 6..9: tile 1) ----------------
         const int wg = (warp - 2) >> 2;
         const int quarter = warp & 3;
