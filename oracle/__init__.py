@@ -72,6 +72,11 @@ def _load():
         lib.pa_oracle_attend_row.argtypes = [p, p, p, p, p, i64, i64, i32, i32, i32, i32,
                                              i64, i32, dbl, p]
         lib.pa_oracle_attend_row.restype = i32
+        lib.pa_oracle_attend_row_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32, i32,
+                                                   i32, i32, i64, i32, dbl, p]
+        lib.pa_oracle_attend_row_state.restype = i32
+        lib.pa_oracle_merge_states.argtypes = [p, p, p, p, i32, i64, i32]
+        lib.pa_oracle_merge_states.restype = i32
         lib.pa_oracle_paged_attention.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32,
                                                   i32, i32, i64, i32, dbl, i32]
         lib.pa_oracle_paged_attention.restype = i32
@@ -159,6 +164,41 @@ def attend_row(q_row, k_cache, v_cache, block_table_row, seq_len: int, pos: int,
                                   nb, int(window), float(scale), None)
     _check(rc, "attend_row")
     return out
+
+
+def attend_row_state(q_row, k_cache, v_cache, block_table_row, seq_len: int, pos: int,
+                     key_begin: int, num_heads: int, num_kv_heads: int, window: int,
+                     scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """Partial result of one query row over its visible keys j >= key_begin: the row
+    [H, D] and lse [H] (natural log; -inf with a zero row when no key is left)."""
+    lib = _load()
+    q_row, kc, vc = _u16(q_row), _u16(k_cache), _u16(v_cache)
+    bt = _i32(block_table_row)
+    nb, bs, hkv, d = kc.shape
+    out = np.zeros((num_heads, d), dtype=np.float64)
+    lse = np.zeros(num_heads, dtype=np.float64)
+    rc = lib.pa_oracle_attend_row_state(_ptr(out), _ptr(lse), _ptr(q_row), _ptr(kc), _ptr(vc),
+                                        _ptr(bt), int(seq_len), int(pos), int(key_begin),
+                                        num_heads, num_kv_heads, d, bs, nb, int(window),
+                                        float(scale), None)
+    _check(rc, "attend_row_state")
+    return out, lse
+
+
+def merge_states(states, lses) -> tuple[np.ndarray, np.ndarray]:
+    """Merge R partial results: states [R, rows, D], lses [R, rows] (float64).
+    Returns (out [rows, D], lse [rows])."""
+    lib = _load()
+    st = np.ascontiguousarray(states, dtype=np.float64)
+    ls = np.ascontiguousarray(lses, dtype=np.float64)
+    r, rows, d = st.shape
+    if ls.shape != (r, rows):
+        raise ValueError("lses must be [R, rows]")
+    out = np.zeros((rows, d), dtype=np.float64)
+    lse = np.zeros(rows, dtype=np.float64)
+    _check(lib.pa_oracle_merge_states(_ptr(out), _ptr(lse), _ptr(st), _ptr(ls), r, rows, d),
+           "merge_states")
+    return out, lse
 
 
 def paged_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_table,

@@ -34,6 +34,18 @@
  *          paged_attention_decode: o = sum_j softmax_j(scale * q.k_j) v_j over the
  *          visible keys; scale is passed in final form (normally 1/sqrt(head_dim)).
  *
+ *  state   "05 Attention Backends", section 7.1 (split-KV: each slice of a long
+ *          context yields a partial result that is merged afterwards) and section 8
+ *          (cascade attention: a shared prefix is attended once, each request's
+ *          suffix separately, and the two are merged; mathematically equivalent).
+ *          The partial result of a query over a subset J of its visible keys is the
+ *          pair (o_J, lse_J): o_J = sum_{j in J} e^{s_j} v_j / sum_{j in J} e^{s_j}
+ *          and lse_J = ln sum_{j in J} e^{s_j}, with s_j = scale * q.k_j.
+ *  merge   for disjoint subsets J_1..J_R of the visible keys, the attention over
+ *          their union is o = sum_r e^{lse_r} o_r / sum_r e^{lse_r} and
+ *          lse = ln sum_r e^{lse_r} (a subset with no keys has lse = -inf and
+ *          contributes nothing).
+ *
  * Everything is done in fp64 with no tiling, no online softmax and no reordering
  * beyond the plain definition: max, exp, sum, divide.
  *
@@ -126,19 +138,23 @@ int pa_oracle_mask(int sq, int sk, int window, uint8_t *allowed)
 /* ------------------------------------------------------------ attention --- */
 
 /*
- * One query row, all heads.  q_row: [num_heads, head_dim] bf16 bits.
- * out: [num_heads, head_dim] fp64.  block_table_row: this sequence's row of the
- * block table.  seq_len keys, query at absolute position pos (pos < seq_len).
- * work: caller scratch of seq_len doubles (NULL -> allocated here).
+ * One query row, all heads, over the visible keys j >= key_begin.
+ * q_row: [num_heads, head_dim] bf16 bits.  out: [num_heads, head_dim] fp64.
+ * lse: [num_heads] fp64 (may be NULL): ln of the sum of e^{s_j} over those keys,
+ * -inf when there are none (then the output row is zeros).
+ * block_table_row: this sequence's row of the block table.  seq_len keys, query at
+ * absolute position pos (pos < seq_len).  work: caller scratch of seq_len doubles
+ * (NULL -> allocated here).
  */
-int pa_oracle_attend_row(double *out, const uint16_t *q_row, const uint16_t *k_cache,
-                         const uint16_t *v_cache, const int32_t *block_table_row,
-                         int64_t seq_len, int64_t pos, int num_heads, int num_kv_heads,
-                         int head_dim, int block_size, int64_t num_blocks, int window,
-                         double scale, double *work)
+int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
+                               const uint16_t *k_cache, const uint16_t *v_cache,
+                               const int32_t *block_table_row, int64_t seq_len, int64_t pos,
+                               int64_t key_begin, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, int window,
+                               double scale, double *work)
 {
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
-        head_dim <= 0 || block_size <= 0 || seq_len < 0 || pos < 0 ||
+        head_dim <= 0 || block_size <= 0 || seq_len < 0 || pos < 0 || key_begin < 0 ||
         (seq_len > 0 && pos >= seq_len))
         return ORACLE_EINVAL;
     const int group = num_heads / num_kv_heads; /* num_queries_per_kv */
@@ -163,7 +179,7 @@ int pa_oracle_attend_row(double *out, const uint16_t *q_row, const uint16_t *k_c
         /* logits s_j = scale * q . k_j for every visible key j */
         double m = -INFINITY;
         int64_t visible = 0;
-        for (int64_t j = 0; j < seq_len; ++j) {
+        for (int64_t j = key_begin; j < seq_len; ++j) {
             if (!key_visible(pos, j, window))
                 continue;
             const int64_t phys = block_table_row[j / block_size];
@@ -188,13 +204,15 @@ int pa_oracle_attend_row(double *out, const uint16_t *q_row, const uint16_t *k_c
         if (visible == 0) {
             for (int d = 0; d < head_dim; ++d)
                 o[d] = 0.0;
+            if (lse)
+                lse[h] = -INFINITY;
             continue;
         }
         /* softmax weights a_j = exp(s_j - m); o = sum_j a_j v_j / sum_j a_j */
         double denom = 0.0;
         for (int d = 0; d < head_dim; ++d)
             acc[d] = 0.0;
-        for (int64_t j = 0; j < seq_len; ++j) {
+        for (int64_t j = key_begin; j < seq_len; ++j) {
             if (!key_visible(pos, j, window))
                 continue;
             const int64_t phys = block_table_row[j / block_size];
@@ -208,11 +226,64 @@ int pa_oracle_attend_row(double *out, const uint16_t *q_row, const uint16_t *k_c
         }
         for (int d = 0; d < head_dim; ++d)
             o[d] = acc[d] / denom;
+        if (lse)
+            lse[h] = m + log(denom);
     }
     free(acc);
     if (own)
         free(logits);
     return rc;
+}
+
+/* One query row, all heads, over all its visible keys (attend_row_state from key 0). */
+int pa_oracle_attend_row(double *out, const uint16_t *q_row, const uint16_t *k_cache,
+                         const uint16_t *v_cache, const int32_t *block_table_row,
+                         int64_t seq_len, int64_t pos, int num_heads, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, int window,
+                         double scale, double *work)
+{
+    return pa_oracle_attend_row_state(out, NULL, q_row, k_cache, v_cache, block_table_row,
+                                      seq_len, pos, 0, num_heads, num_kv_heads, head_dim,
+                                      block_size, num_blocks, window, scale, work);
+}
+
+/*
+ * Merge R partial results of the same rows (see "merge" above).  states:
+ * [num_states, rows, head_dim], lses: [num_states, rows]; out: [rows, head_dim],
+ * out_lse: [rows] (may be NULL).  Rows whose every part is empty get zeros / -inf.
+ */
+int pa_oracle_merge_states(double *out, double *out_lse, const double *states,
+                           const double *lses, int num_states, int64_t rows, int head_dim)
+{
+    if (num_states <= 0 || rows < 0 || head_dim <= 0)
+        return ORACLE_EINVAL;
+    for (int64_t i = 0; i < rows; ++i) {
+        double m = -INFINITY;
+        for (int r = 0; r < num_states; ++r)
+            if (lses[(int64_t)r * rows + i] > m)
+                m = lses[(int64_t)r * rows + i];
+        double *o = out + i * head_dim;
+        for (int d = 0; d < head_dim; ++d)
+            o[d] = 0.0;
+        if (m == -INFINITY) {
+            if (out_lse)
+                out_lse[i] = -INFINITY;
+            continue;
+        }
+        double denom = 0.0;
+        for (int r = 0; r < num_states; ++r) {
+            const double w = exp(lses[(int64_t)r * rows + i] - m);
+            denom += w;
+            const double *src = states + ((int64_t)r * rows + i) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] += w * src[d];
+        }
+        for (int d = 0; d < head_dim; ++d)
+            o[d] /= denom;
+        if (out_lse)
+            out_lse[i] = m + log(denom);
+    }
+    return ORACLE_OK;
 }
 
 /* Work list shared by the threads of pa_oracle_paged_attention. */

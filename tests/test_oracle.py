@@ -354,3 +354,104 @@ def test_empty_sequence_gives_zero_row_and_bad_block_is_reported():
 def test_thread_count_does_not_change_result():
     case = make_case("varlen_prefill_small", seed=14)
     np.testing.assert_array_equal(_run_oracle(case, num_threads=1), _run_oracle(case, num_threads=5))
+
+
+# ------------------------------------------------------- partial results (state) ---
+# "05 Attention Backends", section 7.1 (split-KV) and section 8 (cascade): attention over
+# a key set may be computed per disjoint part and merged; these pins tie the oracle's
+# state and merge to the plain attention pinned above.
+
+def _state(case, i, key_begin, window=0):
+    w = case.workload
+    sk = int(case.seq_lens[i])
+    return oracle.attend_row_state(bf16_bits(case.q)[case.cu_seqlens_q[i + 1] - 1],
+                                   bf16_bits(case.k_cache), bf16_bits(case.v_cache),
+                                   case.block_table[i], sk, sk - 1, key_begin, w.num_heads,
+                                   w.num_kv_heads, window, w.final_scale)
+
+
+def _state_range(case, i, begin, end):
+    """State of sequence i's last query over keys [begin, end) (no window): a query at
+    position end - 1 of the sequence truncated to `end` keys, from key `begin`."""
+    w = case.workload
+    return oracle.attend_row_state(bf16_bits(case.q)[case.cu_seqlens_q[i + 1] - 1],
+                                   bf16_bits(case.k_cache), bf16_bits(case.v_cache),
+                                   case.block_table[i], end, end - 1, begin, w.num_heads,
+                                   w.num_kv_heads, 0, w.final_scale)
+
+
+def test_state_of_one_key_is_its_value_and_logit():
+    case = _contiguous_case(4, 2, 32, [0], [9], seed=60)
+    o, lse = _state(case, 0, key_begin=8)  # only the last key is left
+    k, v = _contiguous_kv(case, 0)
+    q = case.q.double()[8]
+    G = 2
+    for h in range(4):
+        np.testing.assert_array_equal(o[h], v[8, h // G].numpy())
+        logit = case.workload.final_scale * float((q[h] * k[8, h // G]).sum())
+        assert lse[h] == pytest.approx(logit, rel=0, abs=1e-12)
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_state_of_zero_query_has_lse_log_count(window):
+    case = _contiguous_case(4, 4, 16, [0], [23], seed=61)
+    case.q.zero_()
+    for kb in (0, 7, 22):
+        o, lse = _state(case, 0, key_begin=kb, window=window)
+        lo = max(kb, 23 - window) if window > 0 else kb
+        np.testing.assert_allclose(lse, math.log(23 - lo), rtol=0, atol=1e-12)
+
+
+def test_merging_disjoint_parts_gives_the_whole():
+    w = Workload("st", 8, 2, 32, 16, ())
+    case = make_case_from_lengths(w, [0, 0, 0], [70, 33, 130], seed=62)
+    for i, cuts in ((0, [1, 40]), (1, [16]), (2, [5, 64, 100])):
+        sk = int(case.seq_lens[i])
+        whole, whole_lse = _state(case, i, 0)
+        edges = [0] + cuts + [sk]
+        parts = [_state_range(case, i, a, b) for a, b in zip(edges[:-1], edges[1:])]
+        got, got_lse = oracle.merge_states(np.stack([o for o, _ in parts]),
+                                           np.stack([l for _, l in parts]))
+        np.testing.assert_allclose(got, whole, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(got_lse, whole_lse, rtol=0, atol=1e-12)
+        # The merge does not depend on the order of the parts.
+        got2, _ = oracle.merge_states(np.stack([o for o, _ in parts[::-1]]),
+                                      np.stack([l for _, l in parts[::-1]]))
+        np.testing.assert_allclose(got2, whole, rtol=0, atol=1e-12)
+
+
+def test_merge_treats_empty_parts_as_absent():
+    rng = np.random.default_rng(63)
+    o = rng.standard_normal((1, 5, 8))
+    lse = rng.standard_normal((1, 5))
+    empty_o, empty_l = np.zeros((1, 5, 8)), np.full((1, 5), -np.inf)
+    got, got_lse = oracle.merge_states(np.concatenate([empty_o, o, empty_o]),
+                                       np.concatenate([empty_l, lse, empty_l]))
+    np.testing.assert_allclose(got, o[0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(got_lse, lse[0], rtol=0, atol=1e-15)
+    got, got_lse = oracle.merge_states(np.concatenate([empty_o, empty_o]),
+                                       np.concatenate([empty_l, empty_l]))
+    assert not got.any() and np.isneginf(got_lse).all()
+
+
+def test_shared_prefix_attention_is_prefix_state_merged_with_suffix_state():
+    # Cascade: sequences whose first P keys live in the same physical blocks.
+    w = Workload("cas", 8, 2, 32, 16, ())
+    case = make_case_from_lengths(w, [0, 0, 0], [80, 50, 97], seed=64)
+    P = 48  # three shared blocks
+    case.block_table[1, :3] = case.block_table[0, :3]
+    case.block_table[2, :3] = case.block_table[0, :3]
+    for i in range(3):
+        whole, whole_lse = _state(case, i, 0)
+        o1, l1 = _state_range(case, i, 0, P)
+        o2, l2 = _state(case, i, P)
+        got, got_lse = oracle.merge_states(np.stack([o1, o2]), np.stack([l1, l2]))
+        np.testing.assert_allclose(got, whole, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(got_lse, whole_lse, rtol=0, atol=1e-12)
+    # The prefix state depends only on the shared blocks: same for every sequence
+    # whose query is the same.
+    case.q[case.cu_seqlens_q[2] - 1] = case.q[case.cu_seqlens_q[1] - 1]
+    a, la = _state_range(case, 0, 0, P)
+    b, lb = _state_range(case, 1, 0, P)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
