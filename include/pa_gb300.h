@@ -195,6 +195,52 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *key, const voi
                             int num_splits, void *stream);
 
 /*
+ * pa_decode_state - the partial result of pa_decode over a part of each sequence's keys.
+ * "05 Attention Backends", section 7.1 (split-KV: each slice of a long context gives a
+ * partial result that is merged afterwards) and section 8 (cascade attention: a shared
+ * prefix and each request's suffix are attended separately and combined).
+ *
+ * Same keys as pa_decode (window included), restricted to j >= key_begin[b].  For each
+ * (b, h) it writes the normalised row
+ *     state[b][h] = sum_j e^{s_j} V_j / sum_j e^{s_j},   s_j = scale * q[b][h] . K_j,
+ * and lse[b][h] = ln sum_j e^{s_j}; with no key left: a zero row and lse = -inf.
+ * Partial results of disjoint key sets merge with pa_merge_states.
+ *
+ *   state      [batch, num_heads, head_dim] fp32, device, 16-byte aligned (written)
+ *   lse        [batch, num_heads] fp32, device (written)
+ *   key_begin  [batch] int32, device, or NULL (0): first key position to attend
+ *   workspace  at least pa_decode_state_workspace_size(...) bytes, 256-byte aligned
+ * Other arguments, limits and errors as pa_decode (no new-token store here).
+ */
+size_t pa_decode_state_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                      int max_seq_len, int sliding_window, int num_splits);
+pa_status pa_decode_state(float *state, float *lse, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table, int max_num_blocks,
+                          const int32_t *seq_lens, const int32_t *key_begin, int batch,
+                          int max_seq_len, int64_t num_blocks, int block_size, int num_heads,
+                          int num_kv_heads, int head_dim, int sliding_window, float scale,
+                          int num_splits, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
+ * pa_merge_states - merge partial results of the same rows ("05 Attention Backends",
+ * sections 7.1 and 8; the split-KV combine of pa_decode, exposed).  For each row i:
+ *     lse_i = ln sum_r e^{lses[r][i]},   o_i = sum_r e^{lses[r][i] - lse_i} states[r][i]
+ * Parts with lse = -inf are absent; a row with no part gives zeros and lse = -inf.
+ *
+ *   out        [rows, head_dim] bf16, device, 16-byte aligned, or NULL
+ *   out_state  [rows, head_dim] fp32, device, 16-byte aligned, or NULL
+ *   out_lse    [rows] fp32, device, or NULL (at least one of the three is set)
+ *   states     [num_states, rows, head_dim] fp32, device, 16-byte aligned
+ *   lses       [num_states, rows] fp32, device
+ * A row is one (token, head) pair: rows = tokens * num_heads.  head_dim in {64, 128}.
+ * Asynchronous on `stream`; no allocation.
+ */
+pa_status pa_merge_states(void *out, float *out_state, float *out_lse, const float *states,
+                          const float *lses, int num_states, int64_t rows, int head_dim,
+                          void *stream);
+
+/*
  * pa_varlen_prefill - packed variable-length causal / chunked prefill over the
  * paged cache.  "MinivLLM API docs - Attention", section flash_attention_prefill
  * (varlen packing by cu_seqlens, causal, GQA); "vllm-npu 0.4.2, xformers.py",

@@ -25,6 +25,9 @@ from ._lib import (  # noqa: F401
     load,
     pa_decode,
     pa_decode_noalloc,
+    pa_decode_state,
+    pa_decode_state_workspace_size,
+    pa_merge_states,
     pa_decode_num_splits,
     pa_decode_workspace_size,
     pa_read_device_error,

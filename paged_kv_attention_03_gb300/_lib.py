@@ -29,7 +29,8 @@ DEVERR_SLOT_MISMATCH = 0x40
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
-            "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string")
+            "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string",
+            "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states")
 
 
 class PAError(RuntimeError):
@@ -77,6 +78,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_varlen_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                           i32, i32, i32, i64, i32, i32, i32, i32, i32, f32, vp]
         lib.pa_varlen_prefill.restype = ctypes.c_int
+        lib.pa_decode_state_workspace_size.argtypes = [i32] * 7
+        lib.pa_decode_state_workspace_size.restype = sz
+        lib.pa_decode_state.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i64, i32,
+                                        i32, i32, i32, i32, f32, i32, vp, sz, vp]
+        lib.pa_decode_state.restype = ctypes.c_int
+        lib.pa_merge_states.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32, vp]
+        lib.pa_merge_states.restype = ctypes.c_int
         lib.pa_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pa_read_device_error.restype = ctypes.c_int
         _lib = lib
@@ -188,6 +196,75 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                        head_dim, int(sliding_window), float(scale), int(num_splits), ws_ptr,
                        ws_bytes, _stream(dev))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_state_workspace_size(batch: int, num_heads: int, num_kv_heads: int,
+                                   head_dim: int, max_seq_len: int, sliding_window: int = 0,
+                                   num_splits: int = 0) -> int:
+    return int(load().pa_decode_state_workspace_size(batch, num_heads, num_kv_heads, head_dim,
+                                                     max_seq_len, sliding_window, num_splits))
+
+
+def pa_decode_state(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                    scale: float, sliding_window: int = 0, num_splits: int = 0,
+                    key_begin: torch.Tensor | None = None, state: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Partial decode over keys j >= key_begin[b]: returns (state [B, H, D] fp32,
+    lse [B, H] fp32, natural log)."""
+    lib = load()
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    if key_begin is not None:
+        _need(key_begin, torch.int32, "key_begin", dev)
+    batch, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
+        raise ValueError("pa_decode_state: inconsistent shapes")
+    if state is None:
+        state = torch.empty(batch, num_heads, head_dim, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(batch, num_heads, dtype=torch.float32, device=dev)
+    need = pa_decode_state_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
+                                          sliding_window, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need else 0
+    st = lib.pa_decode_state(_ptr(state), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                             _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                             _ptr(key_begin), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                             head_dim, int(sliding_window), float(scale), int(num_splits),
+                             ws_ptr, ws_bytes, _stream(dev))
+    _check(st, "pa_decode_state")
+    return state, lse
+
+
+def pa_merge_states(states: torch.Tensor, lses: torch.Tensor, out: torch.Tensor | None = None,
+                    out_state: torch.Tensor | None = None, out_lse: torch.Tensor | None = None,
+                    want_bf16: bool = True) -> torch.Tensor | None:
+    """Merge partial results: states [R, ..., D] fp32, lses [R, ...] fp32 (the same rows
+    in every part).  Writes any of out (bf16), out_state (fp32), out_lse; returns out."""
+    lib = load()
+    dev = states.device
+    _need(states, torch.float32, "states", dev)
+    _need(lses, torch.float32, "lses", dev)
+    r = states.shape[0]
+    head_dim = states.shape[-1]
+    rows = states[0].numel() // head_dim
+    if lses.shape[0] != r or lses[0].numel() != rows:
+        raise ValueError("pa_merge_states: states and lses disagree")
+    if out is None and want_bf16:
+        out = torch.empty(states.shape[1:], dtype=torch.bfloat16, device=dev)
+    st = lib.pa_merge_states(_ptr(out), _ptr(out_state), _ptr(out_lse), _ptr(states),
+                             _ptr(lses), r, rows, head_dim, _stream(dev))
+    _check(st, "pa_merge_states")
     return out
 
 

@@ -62,6 +62,12 @@ struct DecodeKernelParams {
     const int32_t *slot_mapping;  // [batch]
     __nv_bfloat16 *kc_w;          // the caches, writable
     __nv_bfloat16 *vc_w;
+    // Partial-state output (null for the normal bf16 output): keys from key_begin[b]
+    // on, result as fp32 rows st_o [batch, num_heads, D] and st_lse [batch, num_heads]
+    // (natural log of the softmax denominator).
+    const int32_t *key_begin;
+    float *st_o;
+    float *st_lse;
     unsigned *err;
 };
 
@@ -73,7 +79,7 @@ struct SeqRange {
 };
 
 __device__ __forceinline__ SeqRange decode_range(int raw_len, int64_t cap, int window,
-                                                 unsigned *err, bool report) {
+                                                 int key_begin, unsigned *err, bool report) {
     SeqRange r;
     int L = raw_len;
     if (L < 0 || static_cast<int64_t>(L) > cap) {
@@ -82,6 +88,7 @@ __device__ __forceinline__ SeqRange decode_range(int raw_len, int64_t cap, int w
     }
     r.L = L;
     r.start = window > 0 ? max(0, L - window) : 0;
+    if (key_begin > r.start) r.start = min(key_begin, L);  // partial state from key_begin
     r.base = r.start & ~15;
     return r;
 }
@@ -111,7 +118,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
     const int lane = threadIdx.x & 31;
 
     const bool report = split == 0 && blockIdx.y == 0 && threadIdx.x == 0;
-    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window, p.err, report);
+    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
+                                     p.key_begin ? p.key_begin[b] : 0, p.err, report);
     const int lo = max(sr.start, sr.base + split * p.chunk);
     const int hi = min(sr.L, sr.base + (split + 1) * p.chunk);
     const int h0 = kvh * p.group + ht * 16;
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
     if (lo >= hi) {
         // Empty split.  A sequence with no keys at all gets a zero row; with several
         // splits the combine kernel writes it.
-        if (p.num_splits == 1 && sr.L == 0) {
+        if (p.ws_o == nullptr && sr.L == 0) {
             for (int i = threadIdx.x; i < rows_valid * D; i += NWARPS * 32)
                 p.out[(static_cast<int64_t>(b) * p.num_heads + h0) * D + i] =
                     __float2bfloat16_rn(0.f);
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
         }
         const float res = acc / L;
         const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h0 + row;
-        if (p.num_splits == 1) {
+        if (p.ws_o == nullptr) {
             p.out[bh * D + d] = __float2bfloat16_rn(res);
         } else {
             p.ws_o[(bh * p.num_splits + split) * D + d] = res;
@@ -440,13 +448,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     const int b = gw / p.num_heads;
     const int h = gw - b * p.num_heads;
     if (b >= batch) return;
-    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window, p.err, false);
-    const int nsplit = sr.L > 0 ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
+    const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
+                                     p.key_begin ? p.key_begin[b] : 0, p.err, false);
+    const int nsplit = sr.L > sr.start ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
     const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h;
     __nv_bfloat16 *dst = p.out + bh * D + lane * PER_LANE;
     if (nsplit == 0) {
+        if (p.st_o != nullptr) {
 #pragma unroll
-        for (int i = 0; i < PER_LANE; ++i) dst[i] = __float2bfloat16_rn(0.f);
+            for (int i = 0; i < PER_LANE; ++i) p.st_o[bh * D + lane * PER_LANE + i] = 0.f;
+            if (lane == 0) p.st_lse[bh] = -INFINITY;
+        } else {
+#pragma unroll
+            for (int i = 0; i < PER_LANE; ++i) dst[i] = __float2bfloat16_rn(0.f);
+        }
         return;
     }
     const float *ml = p.ws_ml + bh * p.num_splits * 2;
@@ -487,6 +502,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     }
     wsum = warp_sum(wsum);
     const float inv = 1.f / wsum;
+    if (p.st_o != nullptr) {
+        // Partial state: normalised row and ln(sum_j e^{s_j}) = (M + log2 wsum) ln 2.
+        float *so = p.st_o + bh * D + lane * PER_LANE;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) so[i] = acc[i] * inv;
+        if (lane == 0) p.st_lse[bh] = (M + log2f(wsum)) * kLn2;
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < PER_LANE; i += 2)
         *reinterpret_cast<__nv_bfloat162 *>(dst + i) =
@@ -513,7 +536,7 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
     e = cudaGetLastError();
-    if (e != cudaSuccess || plan.num_splits == 1) return e;
+    if (e != cudaSuccess || (plan.num_splits == 1 && kp.st_o == nullptr)) return e;
     const int warps = batch * kp.num_heads;
     decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(kp, batch);
     return cudaGetLastError();
@@ -559,8 +582,9 @@ bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int m
     return true;
 }
 
-size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p) {
-    if (p.num_splits <= 1) return 0;
+size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p,
+                              bool state) {
+    if (p.num_splits <= 1 && !state) return 0;  // one split writes its output directly
     const size_t rows = static_cast<size_t>(batch) * num_heads * p.num_splits;
     const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
     return o_bytes + rows * 2 * sizeof(float);
@@ -590,7 +614,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.scale_log2 = a.scale * kLog2e;
     kp.chunk = plan.chunk;
     kp.num_splits = plan.num_splits;
-    if (plan.num_splits > 1) {
+    if (plan.num_splits > 1 || a.state_o != nullptr) {
         const size_t rows = static_cast<size_t>(a.batch) * a.num_heads * plan.num_splits;
         const size_t o_bytes = (rows * a.head_dim * sizeof(float) + 255) / 256 * 256;
         kp.ws_o = static_cast<float *>(a.workspace);
@@ -604,6 +628,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.slot_mapping = a.slot_mapping;
     kp.kc_w = static_cast<__nv_bfloat16 *>(a.k_cache_w);
     kp.vc_w = static_cast<__nv_bfloat16 *>(a.v_cache_w);
+    kp.key_begin = a.key_begin;
+    kp.st_o = a.state_o;
+    kp.st_lse = a.state_lse;
     kp.err = a.err;
     switch (a.head_dim) {
         case 64: return launch_decode_d<64>(kp, plan, a.batch, stream);

@@ -73,7 +73,7 @@ pa_status check_store(const void *key, const void *value, const void *k_cache,
 pa_status run_store(const void *key, const void *value, void *k_cache, void *v_cache,
                     const int32_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
                     int block_size, int num_kv_heads, int head_dim, cudaStream_t stream) {
-    pa::StoreArgs a;
+    pa::StoreArgs a{};
     a.key = key;
     a.value = value;
     a.k_cache = k_cache;
@@ -134,13 +134,17 @@ size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int 
     return pa::decode_workspace_bytes(batch, num_heads, head_dim, plan);
 }
 
-pa_status pa_decode(void *out, const void *q, const void *key, const void *value,
-                    const int32_t *slot_mapping, void *k_cache, void *v_cache,
-                    const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
-                    int batch, int max_seq_len, int64_t num_blocks, int block_size,
-                    int num_heads, int num_kv_heads, int head_dim, int sliding_window,
-                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
-                    void *stream) {
+// pa_decode and pa_decode_state: out (bf16) or state_o / state_lse (partial state).
+static pa_status decode_impl(void *out, float *state_o, float *state_lse,
+                             const int32_t *key_begin, const void *q, const void *key,
+                             const void *value, const int32_t *slot_mapping, void *k_cache,
+                             void *v_cache, const int32_t *block_table, int max_num_blocks,
+                             const int32_t *seq_lens, int batch, int max_seq_len,
+                             int64_t num_blocks, int block_size, int num_heads,
+                             int num_kv_heads, int head_dim, int sliding_window, float scale,
+                             int num_splits, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    const bool state = state_o != nullptr || state_lse != nullptr;
     if (batch < 0 || max_seq_len < 0 || num_blocks < 0 || max_num_blocks < 0 ||
         num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
         return PA_ERR_INVALID_ARG;
@@ -152,16 +156,17 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
     const bool has_new = key || value || slot_mapping;
     if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
     if (batch == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    if (state ? !(state_o && state_lse) : !out) return PA_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
+    if ((out && !aligned16(out)) || (state_o && !aligned16(state_o)) || !aligned16(q) ||
+        !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
     if (max_seq_len > 0 && max_num_blocks == 0) return PA_ERR_INVALID_ARG;
     pa::DecodePlan plan;
     if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
                          num_splits, &plan))
         return PA_ERR_INVALID_ARG;
-    const size_t need = pa::decode_workspace_bytes(batch, num_heads, head_dim, plan);
+    const size_t need = pa::decode_workspace_bytes(batch, num_heads, head_dim, plan, state);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
                      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return PA_ERR_INVALID_ARG;
@@ -171,7 +176,7 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
                                          num_blocks, block_size, num_kv_heads, head_dim);
         if (st != PA_OK) return st;
     }
-    pa::DecodeArgs a;
+    pa::DecodeArgs a{};
     a.out = out;
     a.q = q;
     a.k_cache = k_cache;
@@ -195,8 +200,70 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
     a.slot_mapping = has_new ? slot_mapping : nullptr;
     a.k_cache_w = k_cache;
     a.v_cache_w = v_cache;
+    a.key_begin = key_begin;
+    a.state_o = state_o;
+    a.state_lse = state_lse;
     a.err = device_error_word();
     return from_cuda(pa::launch_decode(a, plan, s));
+}
+
+pa_status pa_decode(void *out, const void *q, const void *key, const void *value,
+                    const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                    const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
+                    int batch, int max_seq_len, int64_t num_blocks, int block_size,
+                    int num_heads, int num_kv_heads, int head_dim, int sliding_window,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    if (out == nullptr && batch > 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, nullptr, nullptr, nullptr, q, key, value, slot_mapping, k_cache,
+                       v_cache, block_table, max_num_blocks, seq_lens, batch, max_seq_len,
+                       num_blocks, block_size, num_heads, num_kv_heads, head_dim,
+                       sliding_window, scale, num_splits, workspace, workspace_bytes, stream);
+}
+
+size_t pa_decode_state_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                      int max_seq_len, int sliding_window, int num_splits) {
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         num_splits, &plan))
+        return 0;
+    return pa::decode_workspace_bytes(batch, num_heads, head_dim, plan, true);
+}
+
+pa_status pa_decode_state(float *state, float *lse, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table, int max_num_blocks,
+                          const int32_t *seq_lens, const int32_t *key_begin, int batch,
+                          int max_seq_len, int64_t num_blocks, int block_size, int num_heads,
+                          int num_kv_heads, int head_dim, int sliding_window, float scale,
+                          int num_splits, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    if (batch > 0 && (state == nullptr || lse == nullptr)) return PA_ERR_INVALID_ARG;
+    return decode_impl(nullptr, state, lse, key_begin, q, nullptr, nullptr, nullptr,
+                       const_cast<void *>(k_cache), const_cast<void *>(v_cache), block_table,
+                       max_num_blocks, seq_lens, batch, max_seq_len, num_blocks, block_size,
+                       num_heads, num_kv_heads, head_dim, sliding_window, scale, num_splits,
+                       workspace, workspace_bytes, stream);
+}
+
+pa_status pa_merge_states(void *out, float *out_state, float *out_lse, const float *states,
+                          const float *lses, int num_states, int64_t rows, int head_dim,
+                          void *stream) {
+    if (num_states <= 0 || rows < 0 || head_dim <= 0) return PA_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (rows == 0) return PA_OK;
+    if (!states || !lses || (!out && !out_state && !out_lse)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(states) || (out && !aligned16(out)) || (out_state && !aligned16(out_state)))
+        return PA_ERR_INVALID_ARG;
+    pa::MergeArgs a{};
+    a.out = out;
+    a.out_state = out_state;
+    a.out_lse = out_lse;
+    a.states = states;
+    a.lses = lses;
+    a.num_states = num_states;
+    a.rows = rows;
+    a.head_dim = head_dim;
+    return from_cuda(pa::launch_merge_states(a, static_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
@@ -236,7 +303,7 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
                                        num_blocks, block_size, num_kv_heads, head_dim, s);
         if (rs != PA_OK) return rs;
     }
-    pa::PrefillArgs a;
+    pa::PrefillArgs a{};
     a.out = out;
     a.q = q;
     a.k_cache = k_cache;

@@ -94,5 +94,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // log2(e): logits are kept in the base-2 domain so exp() becomes exp2().
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 }  // namespace pa

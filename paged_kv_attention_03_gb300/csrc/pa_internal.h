@@ -35,7 +35,9 @@ struct DecodePlan {
 // Returns false on invalid arguments.
 bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seq_len,
                  int sliding_window, int num_splits_request, DecodePlan *plan);
-size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p);
+// state: the call returns partial states (always through the workspace and combine).
+size_t decode_workspace_bytes(int batch, int num_heads, int head_dim, const DecodePlan &p,
+                              bool state = false);
 
 struct DecodeArgs {
     void *out;
@@ -61,6 +63,10 @@ struct DecodeArgs {
     const int32_t *slot_mapping;   // [batch]
     void *k_cache_w;               // the caches, writable
     void *v_cache_w;
+    // Partial-state output (all null for the normal bf16 output).
+    const int32_t *key_begin;      // [batch] first key to attend, or null (0)
+    float *state_o;                // [batch, num_heads, head_dim]
+    float *state_lse;              // [batch, num_heads]
     unsigned *err;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
@@ -90,6 +96,19 @@ struct PrefillArgs {
     unsigned *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// ------------------------------------------------------------ merge_states ---
+struct MergeArgs {
+    void *out;               // [rows, head_dim] bf16, or null
+    float *out_state;        // [rows, head_dim] fp32, or null
+    float *out_lse;          // [rows] fp32, or null
+    const float *states;     // [num_states, rows, head_dim] fp32
+    const float *lses;       // [num_states, rows] fp32
+    int num_states;
+    int64_t rows;
+    int head_dim;
+};
+cudaError_t launch_merge_states(const MergeArgs &a, cudaStream_t stream);
 
 // Map a CUDA error to a pa_status, remembering it for pa_last_cuda_error_string().
 pa_status cuda_status(cudaError_t e);
