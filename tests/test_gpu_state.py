@@ -162,3 +162,14 @@ def test_context_parallel_decode_emulated_on_one_gpu(cuda, ranks):
     assert pa.pa_read_device_error(device=cuda) == 0
     out = pa.pa_merge_states(torch.stack(states), torch.stack(lses))
     assert_parity(out, oracle_attention(case, host_inputs(case)), f"dcp x{ranks}")
+
+
+def test_dcp_decode_single_rank_is_plain_decode(cuda):
+    # Without a process group the context-parallel call is the local decode.
+    from paged_kv_attention_03_gb300.dcp import dcp_decode
+
+    case = _decode_case(cuda, seed=85)
+    L, bt = _t(case.seq_lens, cuda), _t(case.block_table, cuda)
+    out = dcp_decode(case.q, case.k_cache, case.v_cache, bt, L, int(case.seq_lens.max()),
+                     case.workload.final_scale)
+    assert_parity(out, oracle_attention(case, host_inputs(case)), "dcp x1")

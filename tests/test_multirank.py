@@ -68,3 +68,47 @@ def test_reference_arm_prints_one_json_line():
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["unit"] == "GB/s"
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _dcp_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    from paged_kv_attention_03_gb300.dcp import gather_states
+
+    g = torch.Generator().manual_seed(100 + rank)
+    state = torch.randn(3, 4, 8, generator=g)        # [batch, heads, head_dim]
+    lse = torch.randn(3, 4, generator=g) * 5
+    if rank == 1:
+        lse[0, 0] = float("-inf")                    # this rank has no key for one row
+    states, lses = gather_states(state, lse)
+    q.put((rank, state.numpy(), lse.numpy(), states.numpy(), lses.numpy()))
+    torch.distributed.destroy_process_group()
+
+
+def test_context_parallel_exchange_two_ranks():
+    # The exchange step of context-parallel decode: every rank ends with all ranks'
+    # partial results in rank order; merging them is the merge of their key sets.
+    import numpy as np
+    import oracle
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dcp_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in procs), key=lambda x: x[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    own_states = np.stack([r[1] for r in res])
+    own_lses = np.stack([r[2] for r in res])
+    for _, _, _, states, lses in res:
+        np.testing.assert_array_equal(states, own_states)
+        np.testing.assert_array_equal(lses, own_lses)
+    # Row (0, 0) has keys only on rank 0: the merge must return rank 0's row there.
+    merged, merged_lse = oracle.merge_states(own_states.reshape(2, -1, 8).astype(np.float64),
+                                             own_lses.reshape(2, -1).astype(np.float64))
+    np.testing.assert_allclose(merged[0], own_states[0, 0, 0], rtol=0, atol=1e-6)
+    assert merged_lse[0] == pytest.approx(float(own_lses[0, 0, 0]), abs=1e-6)
