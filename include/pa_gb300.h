@@ -241,6 +241,47 @@ pa_status pa_merge_states(void *out, float *out_state, float *out_lse, const flo
                           void *stream);
 
 /*
+ * pa_cascade_decode - decode for a batch whose requests share a cached prefix: the
+ * shared keys are attended once for all requests, each request's own keys apart, and
+ * the two merged.  "05 Attention Backends", section 8 and Q&A 4 (cascade attention:
+ * when the requests of a batch share a long prefix, every query attends the one copy
+ * of the prefix K/V, each request attends its own suffix, and the results combine;
+ * mathematically equivalent, the prefix read once).
+ *
+ * Same result as pa_decode (same arguments, window included, no new-token store) when
+ * the first prefix_len / block_size entries of every row of block_table are equal.
+ * The prefix runs on the tensor cores with the requests' query heads as the rows (one
+ * read of each prefix page per 2 x 128 query rows), the suffix as pa_decode_state from
+ * key prefix_len, and pa_merge_states combines them.
+ *
+ *   prefix_len  shared keys, a multiple of block_size, <= every seq_len (use
+ *               pa_common_prefix_blocks(...) * block_size); 0 gives plain decode
+ *   workspace   at least pa_cascade_decode_workspace_size(...) bytes, 256-byte aligned
+ * Supported: head_dim in {64, 128}; block_size a power of two in [16, 256];
+ * num_heads / num_kv_heads <= 64; scale > 0.
+ */
+size_t pa_cascade_decode_workspace_size(int batch, int num_heads, int num_kv_heads,
+                                        int head_dim, int max_seq_len, int prefix_len,
+                                        int sliding_window);
+pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_table, int max_num_blocks,
+                            const int32_t *seq_lens, int batch, int max_seq_len, int prefix_len,
+                            int64_t num_blocks, int block_size, int num_heads, int num_kv_heads,
+                            int head_dim, int sliding_window, float scale, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * pa_common_prefix_blocks - host-side scan ("05 Attention Backends", Q&A 4: after the
+ * scheduler has fixed the batch it scans the requests' block tables for the longest
+ * common prefix of blocks).  Returns the largest n such that entries 0 .. n-1 are equal
+ * in every row of block_table and n * block_size <= every seq_len; -1 on invalid
+ * arguments.  block_table [batch, max_num_blocks] and seq_lens [batch] are HOST
+ * pointers.
+ */
+int pa_common_prefix_blocks(const int32_t *block_table, int batch, int max_num_blocks,
+                            const int32_t *seq_lens, int block_size);
+
+/*
  * pa_varlen_prefill - packed variable-length causal / chunked prefill over the
  * paged cache.  "MinivLLM API docs - Attention", section flash_attention_prefill
  * (varlen packing by cu_seqlens, causal, GQA); "vllm-npu 0.4.2, xformers.py",

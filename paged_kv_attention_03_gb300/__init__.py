@@ -28,6 +28,9 @@ from ._lib import (  # noqa: F401
     pa_decode_state,
     pa_decode_state_workspace_size,
     pa_merge_states,
+    pa_cascade_decode,
+    pa_cascade_decode_workspace_size,
+    pa_common_prefix_blocks,
     pa_decode_num_splits,
     pa_decode_workspace_size,
     pa_read_device_error,

@@ -30,7 +30,8 @@ DEVERR_SLOT_MISMATCH = 0x40
 EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num_splits",
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
             "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string",
-            "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states")
+            "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states",
+            "pa_cascade_decode_workspace_size", "pa_cascade_decode", "pa_common_prefix_blocks")
 
 
 class PAError(RuntimeError):
@@ -85,6 +86,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_state.restype = ctypes.c_int
         lib.pa_merge_states.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32, vp]
         lib.pa_merge_states.restype = ctypes.c_int
+        lib.pa_cascade_decode_workspace_size.argtypes = [i32] * 7
+        lib.pa_cascade_decode_workspace_size.restype = sz
+        lib.pa_cascade_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32,
+                                          i32, i32, i32, i32, f32, vp, sz, vp]
+        lib.pa_cascade_decode.restype = ctypes.c_int
+        lib.pa_common_prefix_blocks.argtypes = [vp, i32, i32, vp, i32]
+        lib.pa_common_prefix_blocks.restype = ctypes.c_int
         lib.pa_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pa_read_device_error.restype = ctypes.c_int
         _lib = lib
@@ -265,6 +273,60 @@ def pa_merge_states(states: torch.Tensor, lses: torch.Tensor, out: torch.Tensor 
     st = lib.pa_merge_states(_ptr(out), _ptr(out_state), _ptr(out_lse), _ptr(states),
                              _ptr(lses), r, rows, head_dim, _stream(dev))
     _check(st, "pa_merge_states")
+    return out
+
+
+def pa_common_prefix_blocks(block_table, seq_lens, block_size: int) -> int:
+    """Longest run of leading block-table entries shared by every request (host arrays
+    or CPU tensors), limited to whole blocks inside every sequence."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    n = load().pa_common_prefix_blocks(bt.ctypes.data, bt.shape[0], bt.shape[1],
+                                       sl.ctypes.data, int(block_size))
+    if n < 0:
+        raise ValueError("pa_common_prefix_blocks: invalid arguments")
+    return int(n)
+
+
+def pa_cascade_decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int,
+                                     head_dim: int, max_seq_len: int, prefix_len: int,
+                                     sliding_window: int = 0) -> int:
+    return int(load().pa_cascade_decode_workspace_size(batch, num_heads, num_kv_heads,
+                                                       head_dim, max_seq_len, prefix_len,
+                                                       sliding_window))
+
+
+def pa_cascade_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                      prefix_len: int, scale: float, sliding_window: int = 0,
+                      out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode with a prefix shared by every request (the first prefix_len / block_size
+    entries of every block-table row): q [B, H, D] -> out [B, H, D]."""
+    lib = load()
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    batch, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
+        raise ValueError("pa_cascade_decode: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_cascade_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
+                                            prefix_len, sliding_window)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = lib.pa_cascade_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+                               int(max_seq_len), int(prefix_len), nb, bs, num_heads, hkv,
+                               head_dim, int(sliding_window), float(scale), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(dev))
+    _check(st, "pa_cascade_decode")
     return out
 
 

@@ -66,6 +66,7 @@ struct DecodeKernelParams {
     // on, result as fp32 rows st_o [batch, num_heads, D] and st_lse [batch, num_heads]
     // (natural log of the softmax denominator).
     const int32_t *key_begin;
+    int key_begin_all;  // used when key_begin is null
     float *st_o;
     float *st_lse;
     unsigned *err;
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
 
     const bool report = split == 0 && blockIdx.y == 0 && threadIdx.x == 0;
     const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
-                                     p.key_begin ? p.key_begin[b] : 0, p.err, report);
+                                     p.key_begin ? p.key_begin[b] : p.key_begin_all, p.err,
+                                     report);
     const int lo = max(sr.start, sr.base + split * p.chunk);
     const int hi = min(sr.L, sr.base + (split + 1) * p.chunk);
     const int h0 = kvh * p.group + ht * 16;
@@ -449,7 +451,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     const int h = gw - b * p.num_heads;
     if (b >= batch) return;
     const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
-                                     p.key_begin ? p.key_begin[b] : 0, p.err, false);
+                                     p.key_begin ? p.key_begin[b] : p.key_begin_all, p.err,
+                                     false);
     const int nsplit = sr.L > sr.start ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
     const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h;
     __nv_bfloat16 *dst = p.out + bh * D + lane * PER_LANE;
@@ -629,6 +632,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.kc_w = static_cast<__nv_bfloat16 *>(a.k_cache_w);
     kp.vc_w = static_cast<__nv_bfloat16 *>(a.v_cache_w);
     kp.key_begin = a.key_begin;
+    kp.key_begin_all = a.key_begin_all;
     kp.st_o = a.state_o;
     kp.st_lse = a.state_lse;
     kp.err = a.err;

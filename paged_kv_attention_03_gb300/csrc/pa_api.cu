@@ -245,6 +245,165 @@ pa_status pa_decode_state(float *state, float *lse, const void *q, const void *k
                        workspace, workspace_bytes, stream);
 }
 
+// Cascade workspace: R = prefix splits + 1 parts of [rows, head_dim] fp32 and [rows] lse,
+// then the suffix decode's own split-K workspace.
+struct CascadeLayout {
+    int n_splits = 0, chunk_tiles = 1;
+    size_t states = 0, lses = 0, decode_ws = 0, decode_need = 0, total = 0;
+};
+
+static bool cascade_layout(int batch, int num_heads, int num_kv_heads, int head_dim,
+                           int max_seq_len, int prefix_len, int sliding_window,
+                           CascadeLayout *c) {
+    pa::plan_prefix_splits(batch, num_heads, num_kv_heads, prefix_len, &c->n_splits,
+                           &c->chunk_tiles);
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         0, &plan))
+        return false;
+    const size_t rows = static_cast<size_t>(batch) * num_heads;
+    const size_t parts = static_cast<size_t>(c->n_splits) + 1;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    c->states = 0;
+    c->lses = up(parts * rows * head_dim * sizeof(float));
+    c->decode_ws = c->lses + up(parts * rows * sizeof(float));
+    c->decode_need = pa::decode_workspace_bytes(batch, num_heads, head_dim, plan, true);
+    c->total = c->decode_ws + up(c->decode_need);
+    return true;
+}
+
+size_t pa_cascade_decode_workspace_size(int batch, int num_heads, int num_kv_heads,
+                                        int head_dim, int max_seq_len, int prefix_len,
+                                        int sliding_window) {
+    if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || prefix_len < 0 ||
+        num_heads % num_kv_heads != 0)
+        return 0;
+    CascadeLayout c;
+    if (!cascade_layout(batch, num_heads, num_kv_heads, head_dim, max_seq_len, prefix_len,
+                        sliding_window, &c))
+        return 0;
+    return c.total;
+}
+
+pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_table, int max_num_blocks,
+                            const int32_t *seq_lens, int batch, int max_seq_len, int prefix_len,
+                            int64_t num_blocks, int block_size, int num_heads, int num_kv_heads,
+                            int head_dim, int sliding_window, float scale, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    if (batch < 0 || max_seq_len < 0 || num_blocks < 0 || max_num_blocks < 0 ||
+        num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        prefix_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
+    if (batch > 65535) return PA_ERR_UNSUPPORTED;
+    if (prefix_len % block_size != 0 || prefix_len > max_seq_len ||
+        prefix_len / block_size > max_num_blocks)
+        return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    CascadeLayout c;
+    if (!cascade_layout(batch, num_heads, num_kv_heads, head_dim, max_seq_len, prefix_len,
+                        sliding_window, &c))
+        return PA_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < c.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *states = reinterpret_cast<float *>(ws + c.states);
+    float *lses = reinterpret_cast<float *>(ws + c.lses);
+    const int64_t rows = static_cast<int64_t>(batch) * num_heads;
+    unsigned *err = device_error_word();
+    // 1. The prefix, attended once for every request: parts 0 .. n_splits - 1.
+    if (c.n_splits > 0) {
+        pa::PrefixArgs pr{};
+        pr.q = q;
+        pr.k_cache = k_cache;
+        pr.v_cache = v_cache;
+        pr.block_table = block_table;  // row 0 holds the shared prefix blocks
+        pr.req_lens = seq_lens;
+        pr.num_req = batch;
+        pr.prefix_len = prefix_len;
+        pr.num_blocks = num_blocks;
+        pr.block_size = block_size;
+        pr.num_heads = num_heads;
+        pr.num_kv_heads = num_kv_heads;
+        pr.head_dim = head_dim;
+        pr.sliding_window = sliding_window;
+        pr.scale = scale;
+        pr.st_o = states;
+        pr.st_lse = lses;
+        pr.n_splits = c.n_splits;
+        pr.chunk_tiles = c.chunk_tiles;
+        pr.err = err;
+        const pa_status st = from_cuda(pa::launch_prefix_states(pr, s));
+        if (st != PA_OK) return st;
+    }
+    // 2. Each request's suffix (keys from prefix_len on): the last part.
+    pa::DecodePlan plan;
+    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
+                         0, &plan))
+        return PA_ERR_INVALID_ARG;
+    pa::DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.max_num_blocks = max_num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.max_seq_len = max_seq_len;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.sliding_window = sliding_window;
+    a.scale = scale;
+    a.workspace = ws + c.decode_ws;
+    a.key_begin_all = prefix_len;
+    a.state_o = states + static_cast<int64_t>(c.n_splits) * rows * head_dim;
+    a.state_lse = lses + static_cast<int64_t>(c.n_splits) * rows;
+    a.err = err;
+    pa_status st = from_cuda(pa::launch_decode(a, plan, s));
+    if (st != PA_OK) return st;
+    // 3. Merge the parts.
+    pa::MergeArgs m{};
+    m.out = out;
+    m.states = states;
+    m.lses = lses;
+    m.num_states = c.n_splits + 1;
+    m.rows = rows;
+    m.head_dim = head_dim;
+    return from_cuda(pa::launch_merge_states(m, s));
+}
+
+int pa_common_prefix_blocks(const int32_t *block_table, int batch, int max_num_blocks,
+                            const int32_t *seq_lens, int block_size) {
+    if (batch < 0 || max_num_blocks < 0 || block_size <= 0) return -1;
+    if (batch == 0 || block_table == nullptr || seq_lens == nullptr) return 0;
+    int64_t n = max_num_blocks;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t covered = seq_lens[b] > 0 ? seq_lens[b] / block_size : 0;  // whole blocks
+        if (covered < n) n = covered;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t blk = block_table[i];
+        for (int b = 1; b < batch; ++b) {
+            if (block_table[static_cast<int64_t>(b) * max_num_blocks + i] != blk) return static_cast<int>(i);
+        }
+    }
+    return static_cast<int>(n);
+}
+
 pa_status pa_merge_states(void *out, float *out_state, float *out_lse, const float *states,
                           const float *lses, int num_states, int64_t rows, int head_dim,
                           void *stream) {

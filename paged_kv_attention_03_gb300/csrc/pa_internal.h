@@ -64,7 +64,8 @@ struct DecodeArgs {
     void *k_cache_w;               // the caches, writable
     void *v_cache_w;
     // Partial-state output (all null for the normal bf16 output).
-    const int32_t *key_begin;      // [batch] first key to attend, or null (0)
+    const int32_t *key_begin;      // [batch] first key to attend, or null (key_begin_all)
+    int key_begin_all;
     float *state_o;                // [batch, num_heads, head_dim]
     float *state_lse;              // [batch, num_heads]
     unsigned *err;
@@ -96,6 +97,34 @@ struct PrefillArgs {
     unsigned *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Shared-prefix (cascade) partial states: every request's decode query against the
+// prefix_len keys in the first prefix_len / block_size entries of block_table, split
+// into n_splits parts of chunk_tiles 128-key tiles.
+struct PrefixArgs {
+    const void *q;             // [num_req, num_heads, head_dim] bf16
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_table;  // the prefix blocks (a row of the table)
+    const int32_t *req_lens;     // [num_req] seq_lens (window bound)
+    int num_req;
+    int prefix_len;              // multiple of block_size
+    int64_t num_blocks;
+    int block_size;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int sliding_window;
+    float scale;
+    float *st_o;                 // [n_splits, num_req * num_heads, head_dim]
+    float *st_lse;               // [n_splits, num_req * num_heads]
+    int n_splits;
+    int chunk_tiles;
+    unsigned *err;
+};
+void plan_prefix_splits(int num_req, int num_heads, int num_kv_heads, int prefix_len,
+                        int *n_splits, int *chunk_tiles);
+cudaError_t launch_prefix_states(const PrefixArgs &a, cudaStream_t stream);
 
 // ------------------------------------------------------------ merge_states ---
 struct MergeArgs {

@@ -89,6 +89,16 @@ struct PrefillKernelParams {
     int tok_per_tile;  // floor(128 / group)
     int window;
     float scale_log2;  // scale * log2(e) > 0
+    // Shared-prefix mode (cascade): the rows are the decode queries of num_req requests,
+    // the keys the prefix_len keys of block_table row 0; the result of each split of
+    // chunk_tiles key tiles is a partial state: st_o [n_splits, num_req * H, HD] fp32 and
+    // st_lse [n_splits, num_req * H] (natural log).  req_lens bounds the window.
+    const int32_t *req_lens;
+    float *st_o;
+    float *st_lse;
+    int num_req;
+    int prefix_len;
+    int chunk_tiles;
     unsigned *err;
 };
 
@@ -125,10 +135,39 @@ struct Item {
     bool valid;
     bool has1;  // the second query tile has rows
     int seq, kvh, q0, rows0, rows1, q_start, sq, sk, kt0, n_tiles;
+    int split;  // shared-prefix mode: key split of the item
 };
 
+// PREFIX: the shared-prefix (cascade) mode; item idx = (split, query-tile pair, kv head),
+// the requests play the tokens of one sequence whose keys are the prefix.
+template <bool PREFIX>
 __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, bool report) {
     Item it;
+    it.split = 0;
+    if constexpr (PREFIX) {
+        const int per_s = p.num_kv_heads * p.q_items;
+        it.split = idx / per_s;
+        const int rem = idx - it.split * per_s;
+        const int qi = rem / p.num_kv_heads;
+        it.kvh = rem - qi * p.num_kv_heads;
+        it.seq = 0;
+        it.q_start = 0;
+        it.sq = p.num_req;
+        it.sk = p.prefix_len;
+        it.valid = false;
+        it.has1 = false;
+        const int T = p.tok_per_tile;
+        it.q0 = qi * 2 * T;
+        if (it.q0 >= it.sq) return it;
+        it.rows0 = min(T, it.sq - it.q0);
+        it.rows1 = max(0, min(T, it.sq - it.q0 - T));
+        it.has1 = it.rows1 > 0;
+        const int total_tiles = (p.prefix_len + BN - 1) / BN;
+        it.kt0 = it.split * p.chunk_tiles;
+        it.n_tiles = min(p.chunk_tiles, total_tiles - it.kt0);
+        it.valid = it.n_tiles > 0;
+        return it;
+    }
     const int per_q = p.num_kv_heads * p.num_seqs;
     const int qi = p.q_items - 1 - idx / per_q;  // longest-running items first
     const int rem = idx - (idx / per_q) * per_q;
@@ -219,7 +258,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-template <int HD>
+template <int HD, bool PREFIX>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillKernelParams p) {
     using L = Layout<HD>;
@@ -308,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t t = 0, ic = 0;
             bool ok = true;
             int idx = blockIdx.x;
-            Item it = get_item(p, idx, false);
+            Item it = get_item<PREFIX>(p, idx, false);
             while (ok && idx < p.n_items) {
                 if (!it.valid) {
                     idx += gridDim.x;
-                    if (idx < p.n_items) it = get_item(p, idx, false);
+                    if (idx < p.n_items) it = get_item<PREFIX>(p, idx, false);
                     continue;
                 }
                 // Look ahead to the next valid item and pull its Q into L2.
@@ -320,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item nit;
                 nit.valid = false;
                 while (nidx < p.n_items) {
-                    nit = get_item(p, nidx, false);
+                    nit = get_item<PREFIX>(p, nidx, false);
                     if (nit.valid) break;
                     nidx += gridDim.x;
                 }
@@ -365,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t t = 0;
             bool ok = true;
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item(p, idx, true);
+                const Item it = get_item<PREFIX>(p, idx, true);
                 if (!it.valid) continue;
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSV;
@@ -431,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item(p, idx, false);
+                const Item it = get_item<PREFIX>(p, idx, false);
                 if (!it.valid) continue;
                 // Finish the previous item before waiting for this item's Q, so its
                 // epilogue never waits on a Q load.
@@ -485,15 +524,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t c = 0;    // tiles this warpgroup has processed
         bool ok = true;
         for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-            const Item it = get_item(p, idx, false);
+            const Item it = get_item<PREFIX>(p, idx, false);
             if (!it.valid) continue;
             if (wg == 1 && !it.has1) {
                 gt += it.n_tiles;
                 continue;
             }
             const bool valid = row_in_tile && tok < it.rows0 + it.rows1;
-            const int pos = it.sk - it.sq + it.q0 + tok;
-            const int lo = w > 0 ? pos - w + 1 : INT_MIN;
+            int pos, lo;
+            if constexpr (PREFIX) {
+                // Every prefix key is before the request's query; a window drops those
+                // before the request's last w keys.
+                pos = it.sk - 1;
+                const int req_len = p.req_lens[min(it.q0 + tok, p.num_req - 1)];
+                lo = w > 0 ? req_len - w : INT_MIN;
+            } else {
+                pos = it.sk - it.sq + it.q0 + tok;
+                lo = w > 0 ? pos - w + 1 : INT_MIN;
+            }
             float m_ref = -INFINITY;  // reference max (base-2 units) the weights use
             float l_sum = 0.f;
             for (int j = 0; j < it.n_tiles; ++j, ++gt, ++c) {
@@ -608,6 +656,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            if constexpr (PREFIX) {
+                // Partial state of this key split: fp32 row and ln of its denominator.
+                const int64_t rows = static_cast<int64_t>(p.num_req) * p.num_heads;
+                const int64_t r = static_cast<int64_t>(it.q0 + tok) * p.num_heads +
+                                  it.kvh * G + g;
+                float *so = p.st_o + (static_cast<int64_t>(it.split) * rows + r) * HD;
+#pragma unroll 1
+                for (int cc = 0; cc < HD / 32; ++cc) {
+                    float o[32];
+                    tmem_ld_32x32b_x32(ocol + cc * 32, o);
+                    tmem_wait_ld_regs(o);
+                    if (valid) {
+                        float4 *d4 = reinterpret_cast<float4 *>(so + cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv,
+                                                o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+                    }
+                }
+                if (valid) {
+                    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                    p.st_lse[static_cast<int64_t>(it.split) * rows + r] =
+                        l_sum > 0.f ? (m_use + log2f(l_sum)) * kLn2 : -INFINITY;
+                }
+                tc_fence_before();
+                continue;
+            }
             __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(it.q_start + it.q0 + tok) *
                                               p.num_heads + it.kvh * G + g) * HD;
 #pragma unroll 1
@@ -693,7 +768,7 @@ int sm_count() {
     return n;
 }
 
-template <int HD>
+template <int HD, bool PREFIX>
 cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cudaStream_t stream) {
     using L = Layout<HD>;
     const int64_t slots = a.num_blocks * a.block_size;
@@ -706,7 +781,7 @@ cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cuda
     if (!encode_3d(&kp.tmap_v, a.v_cache, HD, a.num_kv_heads, static_cast<uint64_t>(slots),
                    HD * 2ull, static_cast<uint64_t>(a.num_kv_heads) * HD * 2ull, 64, 1, 16))
         return cudaErrorInvalidValue;
-    auto kern = prefill_kernel<HD>;
+    auto kern = prefill_kernel<HD, PREFIX>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
@@ -751,8 +826,74 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.scale_log2 = a.scale * kLog2e;
     kp.err = a.err;
     switch (a.head_dim) {
-        case 64: return launch_prefill_d<64>(kp, a, stream);
-        case 128: return launch_prefill_d<128>(kp, a, stream);
+        case 64: return launch_prefill_d<64, false>(kp, a, stream);
+        case 128: return launch_prefill_d<128, false>(kp, a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+void plan_prefix_splits(int num_req, int num_heads, int num_kv_heads, int prefix_len,
+                        int *n_splits, int *chunk_tiles) {
+    const int group = num_heads / num_kv_heads;
+    const int tok = BM / (group > 0 ? group : 1);
+    const int q_items = (num_req + 2 * tok - 1) / (2 * tok);
+    const int tiles = (prefix_len + BN - 1) / BN;
+    const int per_split = q_items * num_kv_heads;
+    // Enough key splits that the items cover every SM once, at least one tile each.
+    int want = (sm_count() + per_split - 1) / (per_split > 0 ? per_split : 1);
+    if (want < 1) want = 1;
+    if (want > tiles) want = tiles;
+    const int chunk = tiles > 0 ? (tiles + want - 1) / want : 1;
+    *chunk_tiles = chunk;
+    *n_splits = tiles > 0 ? (tiles + chunk - 1) / chunk : 0;
+}
+
+cudaError_t launch_prefix_states(const PrefixArgs &a, cudaStream_t stream) {
+    if (a.num_req == 0 || a.n_splits == 0) return cudaSuccess;
+    const int64_t slots = a.num_blocks * a.block_size;
+    if (slots > 0x7fffffffLL - 256 || a.num_req > 0x7fffffff - 256) return cudaErrorInvalidValue;
+    PrefillKernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    kp.block_table = a.block_table;
+    kp.max_num_blocks = a.prefix_len / a.block_size;
+    kp.num_seqs = 1;
+    int log2_bs = 0;
+    while ((1 << log2_bs) < a.block_size) ++log2_bs;
+    kp.log2_bs = log2_bs;
+    kp.seq_cap = a.prefix_len;
+    kp.num_blocks = a.num_blocks;
+    kp.num_heads = a.num_heads;
+    kp.num_kv_heads = a.num_kv_heads;
+    kp.group = a.num_heads / a.num_kv_heads;
+    kp.tok_per_tile = BM / kp.group;
+    kp.q_items = (a.num_req + 2 * kp.tok_per_tile - 1) / (2 * kp.tok_per_tile);
+    kp.max_seqlen_q = a.num_req;
+    const int64_t n_items = static_cast<int64_t>(a.n_splits) * kp.q_items * a.num_kv_heads;
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kp.n_items = static_cast<int>(n_items);
+    kp.window = a.sliding_window;
+    kp.scale_log2 = a.scale * kLog2e;
+    kp.req_lens = a.req_lens;
+    kp.st_o = a.st_o;
+    kp.st_lse = a.st_lse;
+    kp.num_req = a.num_req;
+    kp.prefix_len = a.prefix_len;
+    kp.chunk_tiles = a.chunk_tiles;
+    kp.err = a.err;
+    // The launcher's view of the call: requests as the tokens of one sequence.
+    PrefillArgs pa_{};
+    pa_.q = a.q;
+    pa_.k_cache = a.k_cache;
+    pa_.v_cache = a.v_cache;
+    pa_.total_q = a.num_req;
+    pa_.num_blocks = a.num_blocks;
+    pa_.block_size = a.block_size;
+    pa_.num_heads = a.num_heads;
+    pa_.num_kv_heads = a.num_kv_heads;
+    pa_.head_dim = a.head_dim;
+    switch (a.head_dim) {
+        case 64: return launch_prefill_d<64, true>(kp, pa_, stream);
+        case 128: return launch_prefill_d<128, true>(kp, pa_, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -134,3 +134,37 @@ def test_read_device_error_without_gpu_reports_cuda_error(lib):
     assert text and text != "no error"
     with pytest.raises(pa.PAError, match=r"PA_ERR_CUDA \(.+\)"):
         raise pa.PAError(pa.PA_ERR_CUDA, "probe")
+
+
+def test_common_prefix_blocks_matches_brute_force():
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        batch = int(rng.integers(1, 6))
+        mb = int(rng.integers(1, 9))
+        bs = 16
+        base = rng.integers(0, 50, size=mb)
+        bt = np.tile(base, (batch, 1)).astype(np.int32)
+        for b in range(1, batch):  # each row diverges somewhere (or never)
+            k = int(rng.integers(0, mb + 1))
+            if k < mb:
+                bt[b, k:] = rng.integers(50, 100, size=mb - k)
+        sl = rng.integers(0, mb * bs + 1, size=batch).astype(np.int32)
+        want = 0
+        while (want < mb and all(bt[b, want] == bt[0, want] for b in range(batch))
+               and all((want + 1) * bs <= sl[b] for b in range(batch))):
+            want += 1
+        assert pa.pa_common_prefix_blocks(bt, sl, bs) == want, (bt, sl)
+
+
+def test_cascade_argument_checks(lib):
+    # prefix_len must be a multiple of block_size and within max_seq_len (host checks).
+    p = ctypes.c_void_p(16)
+    bad = lib.pa_cascade_decode(p, p, p, p, p, 4, p, 2, 100, 17, 10, 16, 8, 2, 128, 0,
+                                ctypes.c_float(0.1), p, 1 << 20, None)
+    assert bad == pa.PA_ERR_INVALID_ARG
+    bad = lib.pa_cascade_decode(p, p, p, p, p, 4, p, 2, 100, 112, 10, 16, 8, 2, 128, 0,
+                                ctypes.c_float(0.1), p, 1 << 20, None)
+    assert bad == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_cascade_decode(p, p, p, p, p, 4, p, 2, 100, 16, 10, 8, 8, 2, 128, 0,
+                                 ctypes.c_float(0.1), p, 1 << 20, None) == pa.PA_ERR_UNSUPPORTED
