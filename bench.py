@@ -312,6 +312,48 @@ class MixedRunner:
         self.dec.step()
 
 
+class CascadeRunner:
+    """64 decode requests sharing a 4096-token cached prefix (one system prompt), each
+    with its own suffix of U[128, 1024] tokens; 32/8 heads, D=128, bs=16."""
+
+    PREFIX_BLOCKS = 256
+
+    def __init__(self, device, seed):
+        import paged_kv_attention_03_gb300 as pa
+        from paged_kv_attention_03_gb300.inputs import Workload, make_shared_prefix_case
+
+        self.pa = pa
+        w = Workload("shared_prefix", 32, 8, 128, 16, ())
+        rng = np.random.default_rng(seed)
+        suffix = rng.integers(128, 1025, size=64)
+        self.case = make_shared_prefix_case(w, self.PREFIX_BLOCKS, suffix, seed, device)
+        c = self.case
+        t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=device)
+        self.bt, self.sl = t(c.block_table), t(c.seq_lens)
+        self.max_len = int(c.seq_lens.max())
+        self.prefix = self.PREFIX_BLOCKS * w.block_size
+        self.out = torch.empty_like(c.q)
+        self.ws = torch.empty(pa.pa_cascade_decode_workspace_size(64, 32, 8, 128, self.max_len,
+                                                                  self.prefix, 0),
+                              dtype=torch.uint8, device=device)
+        need = pa.pa_decode_workspace_size(64, 32, 8, 128, self.max_len, 0, 0)
+        self.dws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        row = w.num_kv_heads * w.head_dim * 2 * 2  # K + V bytes of one key
+        self.logical_bytes = int(c.seq_lens.sum()) * row
+        self.physical_bytes = (self.prefix + int(suffix.sum())) * row
+
+    def cascade(self):
+        c = self.case
+        self.pa.pa_cascade_decode(c.q, c.k_cache, c.v_cache, self.bt, self.sl, self.max_len,
+                                  self.prefix, c.workload.final_scale, 0, out=self.out,
+                                  workspace=self.ws)
+
+    def plain(self):
+        c = self.case
+        self.pa.pa_decode(c.q, c.k_cache, c.v_cache, self.bt, self.sl, self.max_len,
+                          c.workload.final_scale, 0, 0, out=self.out, workspace=self.dws)
+
+
 def _time_steps(fn, steps, warmup, flush, stream):
     """Per-step device time (ms) with CUDA events on `stream`, L2 flushed (untimed) before
     each step."""
@@ -437,6 +479,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
                     help="decode: the decode step only; prefill: the prefill step only "
                          "(profiling runs); both: the full JSON line")
@@ -526,6 +569,9 @@ def main():
     mixed = None
     if not args.no_mixed:
         mixed = _mixed_leg(pa, dev, rank, peaks, flush, stream, args)
+    cascade = None
+    if not args.no_cascade:
+        cascade = _cascade_leg(pa, dev, rank, peaks, flush, stream, args)
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and args.gpus == 1:
@@ -565,7 +611,29 @@ def main():
         line["prefill"] = prefill
     if mixed is not None:
         line["mixed"] = mixed
+    if cascade is not None:
+        line["cascade"] = cascade
     print(json.dumps(line), flush=True)
+
+
+def _cascade_leg(pa, dev, rank, peaks, flush, stream, args):
+    """Shared-prefix decode: cascade vs plain decode on the same batch.  Logical bytes
+    count the prefix once per request (what plain decode reads); physical bytes once."""
+    r = CascadeRunner(dev, 300 + rank)
+    steps = max(20, args.steps // 10)
+    tc = statistics.mean(_time_steps(r.cascade, steps, 3, flush, stream))
+    tp = statistics.mean(_time_steps(r.plain, steps, 3, flush, stream))
+    return {"workload": "shared_prefix: 64 requests, prefix 4096 + own suffix U[128,1024], "
+                        "32/8 heads, D=128, bs=16",
+            "logical_bytes": r.logical_bytes, "physical_bytes": r.physical_bytes,
+            "cascade": {"ms_per_step": round(tc, 4), "launches": 4,
+                        "effective_gbs": round(r.logical_bytes / (tc / 1e3) / 1e9, 1),
+                        "physical_gbs": round(r.physical_bytes / (tc / 1e3) / 1e9, 1),
+                        "physical_frac_of_hbm": round(r.physical_bytes / (tc / 1e3) / 1e9 /
+                                                      peaks["hbm_gbs"], 4)},
+            "plain_decode": {"ms_per_step": round(tp, 4),
+                             "gbs": round(r.logical_bytes / (tp / 1e3) / 1e9, 1)},
+            "speedup": round(tp / tc, 2)}
 
 
 def _mixed_leg(pa, dev, rank, peaks, flush, stream, args):

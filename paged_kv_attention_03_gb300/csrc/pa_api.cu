@@ -245,6 +245,16 @@ pa_status pa_decode_state(float *state, float *lse, const void *q, const void *k
                        workspace, workspace_bytes, stream);
 }
 
+// Split-K plan of the cascade's suffix part: its keys start at prefix_len, so the splits
+// only have to cover the longest suffix.
+static bool suffix_plan(int batch, int num_heads, int num_kv_heads, int head_dim,
+                        int max_seq_len, int prefix_len, int sliding_window,
+                        pa::DecodePlan *plan) {
+    const int span = max_seq_len - prefix_len > 1 ? max_seq_len - prefix_len : 1;
+    return pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, span, sliding_window, 0,
+                           plan);
+}
+
 // Cascade workspace: R = prefix splits + 1 parts of [rows, head_dim] fp32 and [rows] lse,
 // then the suffix decode's own split-K workspace.
 struct CascadeLayout {
@@ -258,8 +268,8 @@ static bool cascade_layout(int batch, int num_heads, int num_kv_heads, int head_
     pa::plan_prefix_splits(batch, num_heads, num_kv_heads, prefix_len, &c->n_splits,
                            &c->chunk_tiles);
     pa::DecodePlan plan;
-    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
-                         0, &plan))
+    if (!suffix_plan(batch, num_heads, num_kv_heads, head_dim, max_seq_len, prefix_len,
+                     sliding_window, &plan))
         return false;
     const size_t rows = static_cast<size_t>(batch) * num_heads;
     const size_t parts = static_cast<size_t>(c->n_splits) + 1;
@@ -349,8 +359,8 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const
     }
     // 2. Each request's suffix (keys from prefix_len on): the last part.
     pa::DecodePlan plan;
-    if (!pa::plan_decode(batch, num_heads, num_kv_heads, head_dim, max_seq_len, sliding_window,
-                         0, &plan))
+    if (!suffix_plan(batch, num_heads, num_kv_heads, head_dim, max_seq_len, prefix_len,
+                     sliding_window, &plan))
         return PA_ERR_INVALID_ARG;
     pa::DecodeArgs a{};
     a.q = q;

@@ -216,6 +216,19 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+def make_shared_prefix_case(w: Workload, prefix_blocks: int, suffix_lens, seed: int = 0,
+                            device: str | torch.device = "cpu") -> PagedCase:
+    """Decode requests whose first `prefix_blocks` cache blocks are the same physical
+    blocks (a cached prefix shared by every request, e.g. one system prompt), each with
+    its own suffix of suffix_lens[b] keys; the query is the last token (seq_len =
+    prefix + suffix).  The blocks each request first held for its prefix stay unused."""
+    prefix = prefix_blocks * w.block_size
+    lens = np.asarray(suffix_lens, dtype=np.int64) + prefix
+    case = make_case_from_lengths(w, list(lens - 1), [1] * len(lens), seed=seed, device=device)
+    case.block_table[1:, :prefix_blocks] = case.block_table[0, :prefix_blocks]
+    return case
+
+
 def split_mixed(case: PagedCase) -> tuple[np.ndarray, np.ndarray]:
     """Indices of the sequences with query_len > 1 and of the decode (query_len == 1) ones."""
     pre = np.nonzero(case.query_lens != 1)[0]

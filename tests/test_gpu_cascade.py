@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import paged_kv_attention_03_gb300 as pa
-from paged_kv_attention_03_gb300.inputs import Workload, make_case_from_lengths
+from paged_kv_attention_03_gb300.inputs import Workload, make_shared_prefix_case
 
 from _parity import assert_parity, host_inputs, oracle_attention
 
@@ -20,11 +20,7 @@ pytestmark = pytest.mark.gpu
 def _shared_case(dev, H, Hkv, D, prefix_blocks, suffix_lens, seed, bs=16):
     """Decode requests whose first prefix_blocks blocks are the same physical blocks."""
     w = Workload("cas", H, Hkv, D, bs, ())
-    P = prefix_blocks * bs
-    lens = np.asarray(suffix_lens) + P
-    case = make_case_from_lengths(w, list(lens - 1), [1] * len(lens), seed=seed, device=dev)
-    case.block_table[1:, :prefix_blocks] = case.block_table[0, :prefix_blocks]
-    return case, P
+    return make_shared_prefix_case(w, prefix_blocks, suffix_lens, seed, dev), prefix_blocks * bs
 
 
 def _cascade(case, dev, P, window=0):
