@@ -77,6 +77,16 @@ def _load():
         lib.pa_oracle_attend_row_state.restype = i32
         lib.pa_oracle_merge_states.argtypes = [p, p, p, p, i32, i64, i32]
         lib.pa_oracle_merge_states.restype = i32
+        lib.pa_oracle_fp8_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.pa_oracle_fp8_e4m3_decode.restype = dbl
+        lib.pa_oracle_fp8_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.pa_oracle_fp8_e4m3_encode.restype = ctypes.c_uint8
+        lib.pa_oracle_store_kvcache_fp8.argtypes = [p, p, p, p, p, i64, i64, i32, i32, i32,
+                                                    ctypes.c_float]
+        lib.pa_oracle_store_kvcache_fp8.restype = i32
+        lib.pa_oracle_paged_attention_fp8.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32,
+                                                      i32, i32, i64, i32, dbl, dbl, i32]
+        lib.pa_oracle_paged_attention_fp8.restype = i32
         lib.pa_oracle_paged_attention.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32,
                                                   i32, i32, i64, i32, dbl, i32]
         lib.pa_oracle_paged_attention.restype = i32
@@ -183,6 +193,52 @@ def attend_row_state(q_row, k_cache, v_cache, block_table_row, seq_len: int, pos
                                         float(scale), None)
     _check(rc, "attend_row_state")
     return out, lse
+
+
+def fp8_e4m3_decode(code: int) -> float:
+    """Value of one FP8 E4M3 code (NaN for S.1111.111)."""
+    return float(_load().pa_oracle_fp8_e4m3_decode(int(code) & 0xFF))
+
+
+def fp8_e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code to the fp32 value x (ties to even, saturating at 448)."""
+    return int(_load().pa_oracle_fp8_e4m3_encode(float(np.float32(x))))
+
+
+def store_kvcache_fp8(key, value, k_cache, v_cache, slot_mapping, block_size: int,
+                      kv_scale: float) -> None:
+    """store_kvcache into FP8 E4M3 caches (uint8 [NB, bs, Hkv, D], in place):
+    code = encode(x / kv_scale) with x the bf16 input and the division in fp32."""
+    lib = _load()
+    key, value = _u16(key), _u16(value)
+    if k_cache.dtype != np.uint8 or v_cache.dtype != np.uint8:
+        raise TypeError("fp8 caches are uint8 arrays")
+    sm = _i32(slot_mapping)
+    t = key.shape[0]
+    nb, bs, hkv, d = k_cache.shape
+    _check(lib.pa_oracle_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(sm), t, nb, bs, hkv, d, float(kv_scale)),
+           "store_kvcache_fp8")
+
+
+def paged_attention_fp8(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_table,
+                        num_heads: int, num_kv_heads: int, window: int, scale: float,
+                        kv_scale: float, num_threads: int = 0) -> np.ndarray:
+    """paged_attention over FP8 E4M3 caches (uint8) whose elements read code * kv_scale."""
+    lib = _load()
+    q = _u16(q)
+    if k_cache.dtype != np.uint8 or v_cache.dtype != np.uint8:
+        raise TypeError("fp8 caches are uint8 arrays")
+    kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
+    cu, sl, bt = _i32(cu_seqlens_q), _i32(seq_lens), _i32(block_table)
+    nb, bs, hkv, d = kc.shape
+    out = np.zeros((q.shape[0], num_heads, d), dtype=np.float64)
+    _check(lib.pa_oracle_paged_attention_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(cu),
+                                             _ptr(sl), _ptr(bt), bt.shape[1], len(sl),
+                                             num_heads, num_kv_heads, d, bs, nb, int(window),
+                                             float(scale), float(kv_scale), num_threads),
+           "paged_attention_fp8")
+    return out
 
 
 def merge_states(states, lses) -> tuple[np.ndarray, np.ndarray]:

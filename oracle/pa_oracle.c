@@ -41,6 +41,11 @@
  *          The partial result of a query over a subset J of its visible keys is the
  *          pair (o_J, lse_J): o_J = sum_{j in J} e^{s_j} v_j / sum_{j in J} e^{s_j}
  *          and lse_J = ln sum_{j in J} e^{s_j}, with s_j = scale * q.k_j.
+ *  fp8     "vllm-npu 0.4.2 wheel diff", torch_sdpa.py / xformers.py: with an fp8 KV cache
+ *          the cache write and the paged attention both take one kv_scale.  Reading
+ *          taken: the cache holds FP8 E4M3 codes of x / kv_scale (the division in fp32,
+ *          round to nearest even onto the E4M3 grid, finite values beyond 448 saturate
+ *          to 448, NaN -> 0x7F) and attention reads code * kv_scale.
  *  merge   for disjoint subsets J_1..J_R of the visible keys, the attention over
  *          their union is o = sum_r e^{lse_r} o_r / sum_r e^{lse_r} and
  *          lse = ln sum_r e^{lse_r} (a subset with no keys has lse = -inf and
@@ -79,6 +84,83 @@ static double bf16_bits_to_double(uint16_t bits)
 }
 
 double pa_oracle_bf16_to_double(uint16_t bits) { return bf16_bits_to_double(bits); }
+
+/*
+ * FP8 E4M3 (the "fn" variant: no infinities): sign, 4 exponent bits with bias 7, 3
+ * mantissa bits.  Exponent field 0 holds the subnormals m/8 * 2^-6; S.1111.111 is NaN;
+ * the largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+double pa_oracle_fp8_e4m3_decode(uint8_t code)
+{
+    const int sign = code >> 7;
+    const int e = (code >> 3) & 15;
+    const int m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = (m / 8.0) * ldexp(1.0, -6);
+    else
+        v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value to x (ties to the even code, i.e. mantissa LSB 0), by search over
+ * the 127 non-negative finite codes; finite |x| > 448 and +-inf saturate to +-448. */
+uint8_t pa_oracle_fp8_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a > 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(pa_oracle_fp8_e4m3_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+/* store_kvcache into an FP8 E4M3 cache: code = encode(x / kv_scale), x the bf16 input
+ * as fp32, the division in fp32. */
+int pa_oracle_store_kvcache_fp8(const uint16_t *key, const uint16_t *value, uint8_t *k_cache,
+                                uint8_t *v_cache, const int32_t *slot_mapping,
+                                int64_t num_tokens, int64_t num_blocks, int block_size,
+                                int num_kv_heads, int head_dim, float kv_scale)
+{
+    if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || !(kv_scale > 0.0f))
+        return ORACLE_EINVAL;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_blocks * block_size)
+            return ORACLE_ERANGE;
+        for (int64_t i = 0; i < row; ++i) {
+            const float k = (float)bf16_bits_to_double(key[t * row + i]) / kv_scale;
+            const float v = (float)bf16_bits_to_double(value[t * row + i]) / kv_scale;
+            k_cache[slot * row + i] = pa_oracle_fp8_e4m3_encode(k);
+            v_cache[slot * row + i] = pa_oracle_fp8_e4m3_encode(v);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* One cache element as fp64: bf16 bits, or an FP8 E4M3 code times kv_scale. */
+static double cache_elem(const void *cache, int fp8, double kv_scale, int64_t idx)
+{
+    if (fp8)
+        return pa_oracle_fp8_e4m3_decode(((const uint8_t *)cache)[idx]) * kv_scale;
+    return bf16_bits_to_double(((const uint16_t *)cache)[idx]);
+}
 
 /* ---------------------------------------------------------------- store --- */
 
@@ -146,12 +228,12 @@ int pa_oracle_mask(int sq, int sk, int window, uint8_t *allowed)
  * absolute position pos (pos < seq_len).  work: caller scratch of seq_len doubles
  * (NULL -> allocated here).
  */
-int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
-                               const uint16_t *k_cache, const uint16_t *v_cache,
-                               const int32_t *block_table_row, int64_t seq_len, int64_t pos,
-                               int64_t key_begin, int num_heads, int num_kv_heads,
-                               int head_dim, int block_size, int64_t num_blocks, int window,
-                               double scale, double *work)
+static int attend_row_impl(double *out, double *lse, const uint16_t *q_row,
+                           const void *k_cache, const void *v_cache, int fp8,
+                           double kv_scale, const int32_t *block_table_row, int64_t seq_len,
+                           int64_t pos, int64_t key_begin, int num_heads, int num_kv_heads,
+                           int head_dim, int block_size, int64_t num_blocks, int window,
+                           double scale, double *work)
 {
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
         head_dim <= 0 || block_size <= 0 || seq_len < 0 || pos < 0 || key_begin < 0 ||
@@ -187,12 +269,11 @@ int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
                 rc = ORACLE_ERANGE;
                 break;
             }
-            const uint16_t *k =
-                k_cache + ((phys * block_size + j % block_size) * num_kv_heads + kvh) *
-                              (int64_t)head_dim;
+            const int64_t k0 =
+                ((phys * block_size + j % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
             double dot = 0.0;
             for (int d = 0; d < head_dim; ++d)
-                dot += bf16_bits_to_double(q[d]) * bf16_bits_to_double(k[d]);
+                dot += bf16_bits_to_double(q[d]) * cache_elem(k_cache, fp8, kv_scale, k0 + d);
             logits[j] = scale * dot;
             if (logits[j] > m)
                 m = logits[j];
@@ -216,13 +297,12 @@ int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
             if (!key_visible(pos, j, window))
                 continue;
             const int64_t phys = block_table_row[j / block_size];
-            const uint16_t *v =
-                v_cache + ((phys * block_size + j % block_size) * num_kv_heads + kvh) *
-                              (int64_t)head_dim;
+            const int64_t v0 =
+                ((phys * block_size + j % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
             const double a = exp(logits[j] - m);
             denom += a;
             for (int d = 0; d < head_dim; ++d)
-                acc[d] += a * bf16_bits_to_double(v[d]);
+                acc[d] += a * cache_elem(v_cache, fp8, kv_scale, v0 + d);
         }
         for (int d = 0; d < head_dim; ++d)
             o[d] = acc[d] / denom;
@@ -233,6 +313,18 @@ int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
     if (own)
         free(logits);
     return rc;
+}
+
+int pa_oracle_attend_row_state(double *out, double *lse, const uint16_t *q_row,
+                               const uint16_t *k_cache, const uint16_t *v_cache,
+                               const int32_t *block_table_row, int64_t seq_len, int64_t pos,
+                               int64_t key_begin, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, int window,
+                               double scale, double *work)
+{
+    return attend_row_impl(out, lse, q_row, k_cache, v_cache, 0, 1.0, block_table_row,
+                           seq_len, pos, key_begin, num_heads, num_kv_heads, head_dim,
+                           block_size, num_blocks, window, scale, work);
 }
 
 /* One query row, all heads, over all its visible keys (attend_row_state from key 0). */
@@ -289,7 +381,10 @@ int pa_oracle_merge_states(double *out, double *out_lse, const double *states,
 /* Work list shared by the threads of pa_oracle_paged_attention. */
 typedef struct {
     double *out;
-    const uint16_t *q, *k_cache, *v_cache;
+    const uint16_t *q;
+    const void *k_cache, *v_cache;
+    int fp8;
+    double kv_scale;
     const int32_t *cu_seqlens_q, *seq_lens, *block_table;
     int64_t max_num_blocks;
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size, window;
@@ -343,9 +438,10 @@ static void *oracle_worker(void *arg)
         const int64_t sk = job->seq_lens[i];
         const int64_t r = t - job->cu_seqlens_q[i];
         const int64_t pos = sk - sq + r; /* bottom-right alignment */
-        const int rc = pa_oracle_attend_row(
-            job->out + t * row_elems, job->q + t * row_elems, job->k_cache, job->v_cache,
-            job->block_table + (int64_t)i * job->max_num_blocks, sk, pos, job->num_heads,
+        const int rc = attend_row_impl(
+            job->out + t * row_elems, NULL, job->q + t * row_elems, job->k_cache,
+            job->v_cache, job->fp8, job->kv_scale,
+            job->block_table + (int64_t)i * job->max_num_blocks, sk, pos, 0, job->num_heads,
             job->num_kv_heads, job->head_dim, job->block_size, job->num_blocks,
             job->window, job->scale, work);
         if (rc != ORACLE_OK) {
@@ -365,13 +461,13 @@ static void *oracle_worker(void *arg)
  * cu_seqlens_q = 0, 1, ..., num_seqs.  q, out: [total_rows, num_heads, head_dim].
  * block_table: [num_seqs, max_num_blocks].  num_threads <= 0 -> all online CPUs.
  */
-int pa_oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
-                              const uint16_t *v_cache, const int32_t *cu_seqlens_q,
-                              const int32_t *seq_lens, const int32_t *block_table,
-                              int64_t max_num_blocks, int num_seqs, int num_heads,
-                              int num_kv_heads, int head_dim, int block_size,
-                              int64_t num_blocks, int window, double scale,
-                              int num_threads)
+static int paged_attention_impl(double *out, const uint16_t *q, const void *k_cache,
+                                const void *v_cache, int fp8, double kv_scale,
+                                const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                const int32_t *block_table, int64_t max_num_blocks,
+                                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int64_t num_blocks, int window, double scale,
+                                int num_threads)
 {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0)
@@ -394,6 +490,8 @@ int pa_oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_
     job.q = q;
     job.k_cache = k_cache;
     job.v_cache = v_cache;
+    job.fp8 = fp8;
+    job.kv_scale = kv_scale;
     job.cu_seqlens_q = cu_seqlens_q;
     job.seq_lens = seq_lens;
     job.block_table = block_table;
@@ -435,6 +533,37 @@ int pa_oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_
     free(threads);
     pthread_mutex_destroy(&job.lock);
     return job.rc;
+}
+
+int pa_oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *cu_seqlens_q,
+                              const int32_t *seq_lens, const int32_t *block_table,
+                              int64_t max_num_blocks, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, int window, double scale,
+                              int num_threads)
+{
+    return paged_attention_impl(out, q, k_cache, v_cache, 0, 1.0, cu_seqlens_q, seq_lens,
+                                block_table, max_num_blocks, num_seqs, num_heads,
+                                num_kv_heads, head_dim, block_size, num_blocks, window, scale,
+                                num_threads);
+}
+
+/* The same over an FP8 E4M3 cache read as code * kv_scale. */
+int pa_oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
+                                  const uint8_t *v_cache, const int32_t *cu_seqlens_q,
+                                  const int32_t *seq_lens, const int32_t *block_table,
+                                  int64_t max_num_blocks, int num_seqs, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, int window, double scale,
+                                  double kv_scale, int num_threads)
+{
+    if (!(kv_scale > 0.0))
+        return ORACLE_EINVAL;
+    return paged_attention_impl(out, q, k_cache, v_cache, 1, kv_scale, cu_seqlens_q, seq_lens,
+                                block_table, max_num_blocks, num_seqs, num_heads,
+                                num_kv_heads, head_dim, block_size, num_blocks, window, scale,
+                                num_threads);
 }
 
 /* Number of threads pa_oracle_paged_attention uses for num_threads <= 0. */

@@ -455,3 +455,83 @@ def test_shared_prefix_attention_is_prefix_state_merged_with_suffix_state():
     b, lb = _state_range(case, 1, 0, P)
     np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(la, lb)
+
+
+# ------------------------------------------------------------------ FP8 E4M3 cache ---
+# The E4M3 ("fn") format: sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+# S.1111.111 = NaN, largest finite 448.  Pinned by its defining values, by torch's own
+# float8_e4m3fn conversion (a library routine) and by round trips.
+
+def test_fp8_decode_defining_values():
+    d = oracle.fp8_e4m3_decode
+    assert d(0x38) == 1.0 and d(0x7E) == 448.0 and d(0xFE) == -448.0
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9 and d(0x08) == 2.0 ** -6
+    assert d(0x00) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+    assert math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+
+
+def test_fp8_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.fp8_e4m3_decode(c) for c in range(256)])
+    finite = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert np.isnan(got[~finite]).all()
+
+
+def test_fp8_encode_round_trips_and_matches_torch():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.fp8_e4m3_encode(oracle.fp8_e4m3_decode(c)) == c
+    rng = np.random.default_rng(70)
+    xs = np.concatenate([rng.standard_normal(3000) * s for s in (1e-3, 0.1, 1, 30, 200)])
+    xs = np.clip(xs, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.fp8_e4m3_encode(x) for x in xs], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_fp8_encode_ties_saturation_and_nan():
+    e = oracle.fp8_e4m3_encode
+    assert e(1.0625) == 0x38 and e(1.1875) == 0x3A    # ties go to the even code
+    assert e(1000.0) == 0x7E and e(-1000.0) == 0xFE and e(float("inf")) == 0x7E
+    assert e(460.0) == 0x7E                             # between 448 and the next grid point
+    assert e(float("nan")) == 0x7F
+
+
+def test_fp8_store_quantises_x_over_scale():
+    w = Workload("f8", 4, 2, 16, 16, ())
+    case = make_case_from_lengths(w, [0], [5], seed=71)
+    kc = np.zeros((case.k_cache.shape[0], 16, 2, 16), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    oracle.store_kvcache_fp8(bf16_bits(case.key), bf16_bits(case.value), kc, vc,
+                             case.slot_mapping, 16, 0.25)
+    k = case.key.float().numpy()
+    for t, slot in enumerate(case.slot_mapping):
+        blk, off = divmod(int(slot), 16)
+        want = (torch.from_numpy((k[t] / np.float32(0.25)).astype(np.float32))
+                .to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        np.testing.assert_array_equal(kc[blk, off], want)
+
+
+def test_fp8_attention_equals_bf16_attention_on_exact_values():
+    # Cache values that are E4M3 codes times kv_scale and also exact bf16: both oracle
+    # paths must give the same result.
+    w = Workload("f8a", 8, 2, 32, 16, ())
+    case = make_case_from_lengths(w, [30, 0], [1, 45], seed=72)
+    rng = np.random.default_rng(73)
+    scale = 0.5
+    codes_k = rng.integers(0, 0x7F, size=case.k_cache.shape, dtype=np.uint8) | \
+        (rng.integers(0, 2, size=case.k_cache.shape, dtype=np.uint8) << 7)
+    codes_v = rng.integers(0, 0x7F, size=case.v_cache.shape, dtype=np.uint8)
+    vals_k = np.vectorize(oracle.fp8_e4m3_decode)(codes_k) * scale
+    vals_v = np.vectorize(oracle.fp8_e4m3_decode)(codes_v) * scale
+    kb = torch.from_numpy(vals_k).to(torch.bfloat16)
+    vb = torch.from_numpy(vals_v).to(torch.bfloat16)
+    assert np.array_equal(kb.double().numpy(), vals_k)  # exact in bf16
+    ref = oracle.paged_attention(bf16_bits(case.q), bf16_bits(kb), bf16_bits(vb),
+                                 case.cu_seqlens_q, case.seq_lens, case.block_table, 8, 2, 0,
+                                 w.final_scale)
+    got = oracle.paged_attention_fp8(bf16_bits(case.q), codes_k, codes_v, case.cu_seqlens_q,
+                                     case.seq_lens, case.block_table, 8, 2, 0, w.final_scale,
+                                     scale)
+    np.testing.assert_array_equal(got, ref)
