@@ -195,6 +195,31 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *key, const voi
                             int num_splits, void *stream);
 
 /*
+ * FP8 E4M3 KV cache.  "vllm-npu 0.4.2 wheel diff", torch_sdpa.py / xformers.py: with an
+ * fp8 cache the cache write (write_to_paged_cache) and paged attention
+ * (forward_decode) take one kv_scale.  Reading taken: the cache holds E4M3 codes
+ * ("fn": no infinities, largest 448) of x / kv_scale -- the division in fp32, then
+ * round to nearest even, finite values beyond 448 saturating -- and attention reads
+ * code * kv_scale.  The caches are [num_blocks, block_size, num_kv_heads, head_dim]
+ * bytes; everything else is as pa_store_kvcache / pa_decode (bf16 q, key, value, out).
+ *
+ * pa_store_kvcache_fp8: the store; num_kv_heads * head_dim must be a multiple of 16.
+ * pa_decode_fp8: the decode (the new tokens, when given, are stored the same way inside
+ *     the launch); workspace as pa_decode_workspace_size.  kv_scale > 0.
+ */
+pa_status pa_store_kvcache_fp8(const void *key, const void *value, void *k_cache,
+                               void *v_cache, const int32_t *slot_mapping, int64_t num_tokens,
+                               int64_t num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, float kv_scale, void *stream);
+pa_status pa_decode_fp8(void *out, const void *q, const void *key, const void *value,
+                        const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                        const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
+                        int batch, int max_seq_len, int64_t num_blocks, int block_size,
+                        int num_heads, int num_kv_heads, int head_dim, int sliding_window,
+                        float scale, float kv_scale, int num_splits, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
  * pa_decode_state - the partial result of pa_decode over a part of each sequence's keys.
  * "05 Attention Backends", section 7.1 (split-KV: each slice of a long context gives a
  * partial result that is merged afterwards) and section 8 (cascade attention: a shared

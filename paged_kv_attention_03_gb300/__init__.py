@@ -31,6 +31,8 @@ from ._lib import (  # noqa: F401
     pa_cascade_decode,
     pa_cascade_decode_workspace_size,
     pa_common_prefix_blocks,
+    pa_decode_fp8,
+    pa_store_kvcache_fp8,
     pa_decode_num_splits,
     pa_decode_workspace_size,
     pa_read_device_error,

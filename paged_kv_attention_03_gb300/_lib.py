@@ -31,7 +31,8 @@ EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num
             "pa_decode_workspace_size", "pa_decode", "pa_varlen_prefill",
             "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string",
             "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states",
-            "pa_cascade_decode_workspace_size", "pa_cascade_decode", "pa_common_prefix_blocks")
+            "pa_cascade_decode_workspace_size", "pa_cascade_decode", "pa_common_prefix_blocks",
+            "pa_store_kvcache_fp8", "pa_decode_fp8")
 
 
 class PAError(RuntimeError):
@@ -93,6 +94,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_cascade_decode.restype = ctypes.c_int
         lib.pa_common_prefix_blocks.argtypes = [vp, i32, i32, vp, i32]
         lib.pa_common_prefix_blocks.restype = ctypes.c_int
+        lib.pa_store_kvcache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, f32,
+                                             vp]
+        lib.pa_store_kvcache_fp8.restype = ctypes.c_int
+        lib.pa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
+                                      i32, i32, i32, i32, i32, f32, f32, i32, vp, sz, vp]
+        lib.pa_decode_fp8.restype = ctypes.c_int
         lib.pa_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         lib.pa_read_device_error.restype = ctypes.c_int
         _lib = lib
@@ -157,6 +164,65 @@ def pa_store_kvcache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tens
     st = lib.pa_store_kvcache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
                               _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d, _stream(dev))
     _check(st, "pa_store_kvcache")
+
+
+def pa_store_kvcache_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                         kv_scale: float) -> None:
+    """Store key/value [T, Hkv, D] bf16 into FP8 E4M3 caches (uint8 [NB, bs, Hkv, D]) as
+    codes of x / kv_scale."""
+    lib = load()
+    dev = k_cache.device
+    _need(key, torch.bfloat16, "key", dev)
+    _need(value, torch.bfloat16, "value", dev)
+    _need(k_cache, torch.uint8, "k_cache", dev)
+    _need(v_cache, torch.uint8, "v_cache", dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    nb, bs, hkv, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or key.shape != value.shape or key.shape[1:] != (hkv, d):
+        raise ValueError("store_kvcache_fp8: inconsistent shapes")
+    if slot_mapping.shape[0] != key.shape[0]:
+        raise ValueError("store_kvcache_fp8: slot_mapping length != number of tokens")
+    st = lib.pa_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d,
+                                  float(kv_scale), _stream(dev))
+    _check(st, "pa_store_kvcache_fp8")
+
+
+def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                  scale: float, kv_scale: float, sliding_window: int = 0, num_splits: int = 0,
+                  key: torch.Tensor | None = None, value: torch.Tensor | None = None,
+                  slot_mapping: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Paged decode over FP8 E4M3 caches (uint8 [NB, bs, Hkv, D], read as code * kv_scale);
+    q / key / value / out bf16.  New tokens, when given, are stored in the same launch."""
+    lib = load()
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    _need(k_cache, torch.uint8, "k_cache", dev)
+    _need(v_cache, torch.uint8, "v_cache", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    batch, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
+        raise ValueError("pa_decode_fp8: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
+                                    sliding_window, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if need else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need else 0
+    st = lib.pa_decode_fp8(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                           _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                           _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                           head_dim, int(sliding_window), float(scale), float(kv_scale),
+                           int(num_splits), ws_ptr, ws_bytes, _stream(dev))
+    _check(st, "pa_decode_fp8")
+    return out
 
 
 def pa_decode_num_splits(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,

@@ -25,6 +25,8 @@
 //    (m, l) to the workspace for decode_combine_kernel.
 #include <math.h>
 
+#include <cuda_fp16.h>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 #include "sm100_ptx.cuh"
@@ -67,6 +69,12 @@ struct DecodeKernelParams {
     // (natural log of the softmax denominator).
     const int32_t *key_begin;
     int key_begin_all;  // used when key_begin is null
+    // FP8 E4M3 cache (the FP8 instantiation): codes, their scale, writable views.
+    const uint8_t *k8;
+    const uint8_t *v8;
+    uint8_t *k8_w;
+    uint8_t *v8_w;
+    float kv_scale;
     float *st_o;
     float *st_lse;
     unsigned *err;
@@ -98,7 +106,26 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-template <int D, int NWARPS, int NSTAGES>
+// Two FP8 E4M3 codes (low byte first) -> bf16x2, exactly: every E4M3 value (at most 4
+// significant bits, exponents 2^-9 .. 2^8) is an f16 and a bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack_bf16x2(f.x, f.y);
+}
+
+// Two fp32 values -> two FP8 E4M3 codes (lo in the low byte): round to nearest even,
+// finite values beyond 448 saturate.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// FP8: the cache holds E4M3 codes (x / kv_scale); tiles are converted to bf16 in shared
+// memory after they land, and kv_scale is applied to the scores (K) and results (V).
+template <int D, int NWARPS, int NSTAGES, bool FP8>
 __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const DecodeKernelParams p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
@@ -108,6 +135,14 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
     constexpr int PASSES = 16 / ROWS_PER_PASS;
     constexpr int KSTEPS = D / 16;
     constexpr int DTILES = D / 8;
+    // FP8 ring: 16-key tiles of D bytes per row; then one bf16 K + V tile per warp.
+    constexpr int TILE8 = 16 * D;
+    constexpr int STAGE8 = 2 * TILE8;
+    constexpr int CPR8 = D / 16;  // 16-byte chunks per fp8 row
+    constexpr int RPP8 = 32 / CPR8;
+    constexpr int PASSES8 = 16 / RPP8;
+    static_assert(!FP8 || NSTAGES * STAGE8 + STAGE_BYTES <= NSTAGES * STAGE_BYTES,
+                  "fp8 ring + conversion tile fit the per-warp share");
 
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -136,11 +171,38 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
         const int slot = p.slot_mapping[b];
         const int64_t num_slots = p.num_blocks << p.log2_bs;
         if (slot >= 0 && slot < num_slots) {
-            if (threadIdx.x < 2 * CPR) {
+            const int64_t src_row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
+            const int64_t dst_row = static_cast<int64_t>(slot) * p.num_kv_heads + kvh;
+            if constexpr (FP8) {
+                // 16 elements per thread: code = E4M3(x / kv_scale), the division in fp32.
+                if (threadIdx.x < 2 * CPR8) {
+                    const int which = threadIdx.x / CPR8;
+                    const int c = threadIdx.x - which * CPR8;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        (which ? p.value : p.key) + src_row * D + c * 16);
+                    uint32_t w[8];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 v = src[h];
+                        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = __fdiv_rn(__uint_as_float(u[k] << 16), p.kv_scale);
+                            const float hi =
+                                __fdiv_rn(__uint_as_float(u[k] & 0xffff0000u), p.kv_scale);
+                            w[h * 4 + k] = f32x2_to_e4m3x2(lo, hi);
+                        }
+                    }
+                    uint4 o;
+                    o.x = w[0] | (w[1] << 16);
+                    o.y = w[2] | (w[3] << 16);
+                    o.z = w[4] | (w[5] << 16);
+                    o.w = w[6] | (w[7] << 16);
+                    *reinterpret_cast<uint4 *>((which ? p.v8_w : p.k8_w) + dst_row * D + c * 16) = o;
+                }
+            } else if (threadIdx.x < 2 * CPR) {
                 const int which = threadIdx.x / CPR;
                 const int c = threadIdx.x - which * CPR;
-                const int64_t src_row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
-                const int64_t dst_row = static_cast<int64_t>(slot) * p.num_kv_heads + kvh;
                 const uint4 v = reinterpret_cast<const uint4 *>((which ? p.value : p.key) +
                                                                 src_row * D)[c];
                 reinterpret_cast<uint4 *>((which ? p.vc_w : p.kc_w) + dst_row * D)[c] = v;
@@ -202,6 +264,34 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
     const int64_t row_stride = static_cast<int64_t>(p.num_kv_heads) * D;
 
     auto issue = [&](int u, int st) {
+        if constexpr (FP8) {
+            // fp8 rows, 16-byte chunks, no swizzle (the conversion reads them in order).
+            const uint32_t sb = stage_base + st * STAGE8;
+            const int c = lane % CPR8;
+            const int rsub = lane / CPR8;
+            const int j0 = u * 16;
+#pragma unroll
+            for (int i = 0; i < PASSES8; ++i) {
+                const int r = i * RPP8 + rsub;
+                const int j = j0 + r;
+                int64_t off = 0;
+                uint32_t nbytes = 0;
+                if (j >= lo && j < hi) {
+                    const int blk = __ldg(bt_row + (j >> p.log2_bs));
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        flag_error(p.err, kErrBlockRange);
+                    } else {
+                        off = (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
+                                   p.num_kv_heads + kvh) * D + c * 16;
+                        nbytes = 16;
+                    }
+                }
+                const uint32_t so = r * D + c * 16;
+                cp_async_16_policy(sb + so, p.k8 + off, nbytes, policy);
+                cp_async_16_policy(sb + TILE8 + so, p.v8 + off, nbytes, policy);
+            }
+            return;
+        }
         const uint32_t sb = stage_base + st * STAGE_BYTES;
         const int c = lane % CPR;
         const int rsub = lane / CPR;
@@ -275,7 +365,42 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
         cp_async_wait<NSTAGES - 1>();
         __syncwarp();
 
-        const uint32_t kb = stage_base + (it % NSTAGES) * STAGE_BYTES;
+        uint32_t kb = stage_base + (it % NSTAGES) * STAGE_BYTES;
+        if constexpr (FP8) {
+            // E4M3 -> bf16 into this warp's conversion tile (same swizzled layout as a
+            // bf16 stage): fp8 chunk c of row r becomes bf16 chunks 2c and 2c + 1.
+            const uint32_t src = stage_base + (it % NSTAGES) * STAGE8;
+            kb = stage_base + NSTAGES * STAGE8;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {  // K then V
+#pragma unroll
+                for (int q = lane; q < 16 * CPR8; q += 32) {
+                    const int r = q / CPR8;
+                    const int c = q - r * CPR8;
+                    uint32_t x0, x1, x2, x3;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                 : "r"(src + t * TILE8 + r * D + c * 16));
+                    const uint32_t xs[4] = {x0, x1, x2, x3};
+                    uint32_t y[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        y[2 * k] = e4m3x2_to_bf16x2(xs[k] & 0xffffu);
+                        y[2 * k + 1] = e4m3x2_to_bf16x2(xs[k] >> 16);
+                    }
+                    const uint32_t dst = kb + t * TILE_BYTES + r * ROWB;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     dst + (((2 * c) ^ (r & 7)) << 4)),
+                                 "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     dst + (((2 * c + 1) ^ (r & 7)) << 4)),
+                                 "r"(y[4]), "r"(y[5]), "r"(y[6]), "r"(y[7])
+                                 : "memory");
+                }
+            }
+            __syncwarp();
+        }
         const uint32_t vb = kb + TILE_BYTES;
 
         // S = Q K^T for 16 keys: two n-tiles of 8 keys, even and odd k-steps in
@@ -424,7 +549,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
             L += f * l_s[w * 16 + row];
             acc += f * o_s[(w * 16 + row) * OSTRIDE + d];
         }
-        const float res = acc / L;
+        float res = acc / L;
+        if constexpr (FP8) res *= p.kv_scale;  // V elements read code * kv_scale
         const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h0 + row;
         if (p.ws_o == nullptr) {
             p.out[bh * D + d] = __float2bfloat16_rn(res);
@@ -527,13 +653,13 @@ constexpr int decode_smem_bytes() {
     return kDecodeWarps * kDecodeStages * 2 * 16 * D * 2;
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan, int batch,
                             cudaStream_t stream) {
     constexpr int smem = decode_smem_bytes<D>();
     static_assert(smem >= (kDecodeWarps * 16 * 2 + kDecodeWarps * 16 * (D + 4)) * 4,
                   "merge area must fit in the stage ring");
-    auto kern = decode_split_kernel<D, kDecodeWarps, kDecodeStages>;
+    auto kern = decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
@@ -636,9 +762,26 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.st_o = a.state_o;
     kp.st_lse = a.state_lse;
     kp.err = a.err;
+    if (a.fp8) {
+        // E4M3 caches: codes read through the byte views, kv_scale on the scores (K) and,
+        // in the kernel, on the results (V).
+        kp.k8 = static_cast<const uint8_t *>(a.k_cache);
+        kp.v8 = static_cast<const uint8_t *>(a.v_cache);
+        kp.k8_w = static_cast<uint8_t *>(a.k_cache_w);
+        kp.v8_w = static_cast<uint8_t *>(a.v_cache_w);
+        kp.kv_scale = a.kv_scale;
+        kp.scale_log2 = a.scale * a.kv_scale * kLog2e;
+        kp.k_cache = nullptr;
+        kp.v_cache = nullptr;
+        switch (a.head_dim) {
+            case 64: return launch_decode_d<64, true>(kp, plan, a.batch, stream);
+            case 128: return launch_decode_d<128, true>(kp, plan, a.batch, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (a.head_dim) {
-        case 64: return launch_decode_d<64>(kp, plan, a.batch, stream);
-        case 128: return launch_decode_d<128>(kp, plan, a.batch, stream);
+        case 64: return launch_decode_d<64, false>(kp, plan, a.batch, stream);
+        case 128: return launch_decode_d<128, false>(kp, plan, a.batch, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -143,8 +143,9 @@ static pa_status decode_impl(void *out, float *state_o, float *state_lse,
                              int64_t num_blocks, int block_size, int num_heads,
                              int num_kv_heads, int head_dim, int sliding_window, float scale,
                              int num_splits, void *workspace, size_t workspace_bytes,
-                             void *stream) {
+                             void *stream, int fp8 = 0, float kv_scale = 1.f) {
     const bool state = state_o != nullptr || state_lse != nullptr;
+    if (fp8 && (!(kv_scale > 0.f) || !(kv_scale < 3.0e38f))) return PA_ERR_INVALID_ARG;
     if (batch < 0 || max_seq_len < 0 || num_blocks < 0 || max_num_blocks < 0 ||
         num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
         return PA_ERR_INVALID_ARG;
@@ -203,6 +204,8 @@ static pa_status decode_impl(void *out, float *state_o, float *state_lse,
     a.key_begin = key_begin;
     a.state_o = state_o;
     a.state_lse = state_lse;
+    a.fp8 = fp8;
+    a.kv_scale = kv_scale;
     a.err = device_error_word();
     return from_cuda(pa::launch_decode(a, plan, s));
 }
@@ -219,6 +222,43 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
                        v_cache, block_table, max_num_blocks, seq_lens, batch, max_seq_len,
                        num_blocks, block_size, num_heads, num_kv_heads, head_dim,
                        sliding_window, scale, num_splits, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_fp8(void *out, const void *q, const void *key, const void *value,
+                        const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                        const int32_t *block_table, int max_num_blocks, const int32_t *seq_lens,
+                        int batch, int max_seq_len, int64_t num_blocks, int block_size,
+                        int num_heads, int num_kv_heads, int head_dim, int sliding_window,
+                        float scale, float kv_scale, int num_splits, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    if (out == nullptr && batch > 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, nullptr, nullptr, nullptr, q, key, value, slot_mapping, k_cache,
+                       v_cache, block_table, max_num_blocks, seq_lens, batch, max_seq_len,
+                       num_blocks, block_size, num_heads, num_kv_heads, head_dim,
+                       sliding_window, scale, num_splits, workspace, workspace_bytes, stream,
+                       1, kv_scale);
+}
+
+pa_status pa_store_kvcache_fp8(const void *key, const void *value, void *k_cache,
+                               void *v_cache, const int32_t *slot_mapping, int64_t num_tokens,
+                               int64_t num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, float kv_scale, void *stream) {
+    if (!(kv_scale > 0.f) || !(kv_scale < 3.0e38f)) return PA_ERR_INVALID_ARG;
+    const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                     num_blocks, block_size, num_kv_heads, head_dim);
+    if (st != PA_OK || num_tokens == 0) return st;
+    if ((static_cast<int64_t>(num_kv_heads) * head_dim) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    pa::StoreArgs a{};
+    a.key = key;
+    a.value = value;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slot_mapping = slot_mapping;
+    a.num_tokens = num_tokens;
+    a.num_slots = num_blocks * block_size;
+    a.row_elems = num_kv_heads * head_dim;
+    a.err = device_error_word();
+    return from_cuda(pa::launch_store_kvcache_fp8(a, kv_scale, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pa_decode_state_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,

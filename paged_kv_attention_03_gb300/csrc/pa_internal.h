@@ -23,6 +23,8 @@ struct StoreArgs {
     unsigned *err;
 };
 cudaError_t launch_store_kvcache(const StoreArgs &a, cudaStream_t stream);
+// FP8 E4M3 cache: k_cache / v_cache are [num_slots, row_elems] bytes (row_elems % 16 == 0).
+cudaError_t launch_store_kvcache_fp8(const StoreArgs &a, float kv_scale, cudaStream_t stream);
 
 // ----------------------------------------------------------------- decode ---
 struct DecodePlan {
@@ -66,6 +68,9 @@ struct DecodeArgs {
     // Partial-state output (all null for the normal bf16 output).
     const int32_t *key_begin;      // [batch] first key to attend, or null (key_begin_all)
     int key_begin_all;
+    // FP8 E4M3 cache: k_cache / v_cache hold codes of x / kv_scale (one byte each).
+    int fp8;
+    float kv_scale;
     float *state_o;                // [batch, num_heads, head_dim]
     float *state_lse;              // [batch, num_heads]
     unsigned *err;

@@ -1,0 +1,102 @@
+"""FP8 E4M3 KV cache on the GPU against the fp64 oracle.
+
+The store is bit-exact (an integer decision taken in fp32 on both sides: x / kv_scale
+correctly rounded, then round to nearest even onto E4M3, saturating at 448).  The
+decode reads code * kv_scale exactly and carries the attention bar (max-abs <= 1e-2,
+mean-abs <= 1e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_03_gb300 as pa
+from paged_kv_attention_03_gb300.inputs import Workload, bf16_bits, make_case_from_lengths
+
+from _parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _t(a, dev):
+    return torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=dev)
+
+
+def _codes_of(cache_bf16, kv_scale):
+    """E4M3 codes of the N(0,1) bf16 cache / kv_scale (test input, as a store would give)."""
+    return (cache_bf16.float().cpu() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("kv_scale", [0.5, 0.03])
+def test_fp8_store_is_bit_exact(cuda, kv_scale):
+    w = Workload("s8", 8, 4, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 10], [300, 77], seed=100, device=cuda)
+    # Spread magnitudes: subnormal range, normal range, ties and saturation (|x| > 448 s).
+    g = torch.Generator(device="cpu").manual_seed(101)
+    mags = torch.tensor([1e-4, 1e-2, 1.0, 20.0, 1000.0])
+    pick = torch.randint(0, 5, case.key.shape, generator=g)
+    case.key.copy_((torch.randn(case.key.shape, generator=g) * mags[pick]).to(torch.bfloat16))
+    case.value.copy_((torch.randn(case.value.shape, generator=g) * mags[pick]).to(torch.bfloat16))
+    kc = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device=cuda)
+    vc = torch.zeros_like(kc)
+    pa.pa_store_kvcache_fp8(case.key, case.value, kc, vc, _t(case.slot_mapping, cuda), kv_scale)
+    assert pa.pa_read_device_error(device=cuda) == 0
+    hk = np.zeros(kc.shape, np.uint8)
+    hv = np.zeros(vc.shape, np.uint8)
+    oracle.store_kvcache_fp8(bf16_bits(case.key), bf16_bits(case.value), hk, hv,
+                             case.slot_mapping, 16, kv_scale)
+    np.testing.assert_array_equal(kc.cpu().numpy(), hk)
+    np.testing.assert_array_equal(vc.cpu().numpy(), hv)
+
+
+def _fp8_case(dev, H, Hkv, D, lens, bs=16, seed=102, kv_scale=0.02):
+    w = Workload("d8", H, Hkv, D, bs, ())
+    case = make_case_from_lengths(w, [n - 1 for n in lens], [1] * len(lens), seed=seed,
+                                  device=dev)
+    return case, _codes_of(case.k_cache, kv_scale), _codes_of(case.v_cache, kv_scale), kv_scale
+
+
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("window", [0, 100])
+def test_fp8_decode_matches_oracle(cuda, splits, window):
+    case, kc, vc, s = _fp8_case(cuda, 32, 8, 128, [1, 17, 500, 2048, 3000])
+    out = pa.pa_decode_fp8(case.q, torch.from_numpy(kc).to(cuda), torch.from_numpy(vc).to(cuda),
+                           _t(case.block_table, cuda), _t(case.seq_lens, cuda),
+                           int(case.seq_lens.max()), case.workload.final_scale, s, window,
+                           splits)
+    assert pa.pa_read_device_error(device=cuda) == 0
+    ref = oracle.paged_attention_fp8(bf16_bits(case.q), kc, vc, case.cu_seqlens_q,
+                                     case.seq_lens, case.block_table, 32, 8, window,
+                                     case.workload.final_scale, s)
+    assert_parity(out, ref, f"fp8 decode splits={splits} window={window}")
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs", [(40, 8, 128, 16), (8, 8, 64, 32), (16, 2, 128, 8)])
+def test_fp8_decode_shapes(cuda, H, Hkv, D, bs):
+    case, kc, vc, s = _fp8_case(cuda, H, Hkv, D, [5, 64, 333], bs=bs, seed=103, kv_scale=0.1)
+    out = pa.pa_decode_fp8(case.q, torch.from_numpy(kc).to(cuda), torch.from_numpy(vc).to(cuda),
+                           _t(case.block_table, cuda), _t(case.seq_lens, cuda),
+                           int(case.seq_lens.max()), case.workload.final_scale, s)
+    ref = oracle.paged_attention_fp8(bf16_bits(case.q), kc, vc, case.cu_seqlens_q,
+                                     case.seq_lens, case.block_table, H, Hkv, 0,
+                                     case.workload.final_scale, s)
+    assert_parity(out, ref, f"fp8 {H}/{Hkv} D={D} bs={bs}")
+
+
+def test_fp8_decode_with_fused_store(cuda):
+    case, kc, vc, s = _fp8_case(cuda, 32, 8, 128, [40, 700, 1], seed=104, kv_scale=0.05)
+    hk, hv = kc.copy(), vc.copy()
+    oracle.store_kvcache_fp8(bf16_bits(case.key), bf16_bits(case.value), hk, hv,
+                             case.slot_mapping, 16, s)
+    dk, dv = torch.from_numpy(kc).to(cuda), torch.from_numpy(vc).to(cuda)
+    out = pa.pa_decode_fp8(case.q, dk, dv, _t(case.block_table, cuda), _t(case.seq_lens, cuda),
+                           int(case.seq_lens.max()), case.workload.final_scale, s,
+                           key=case.key, value=case.value,
+                           slot_mapping=_t(case.slot_mapping, cuda))
+    assert pa.pa_read_device_error(device=cuda) == 0
+    np.testing.assert_array_equal(dk.cpu().numpy(), hk)
+    np.testing.assert_array_equal(dv.cpu().numpy(), hv)
+    ref = oracle.paged_attention_fp8(bf16_bits(case.q), hk, hv, case.cu_seqlens_q,
+                                     case.seq_lens, case.block_table, 32, 8, 0,
+                                     case.workload.final_scale, s)
+    assert_parity(out, ref, "fp8 fused store")
