@@ -480,6 +480,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-cascade", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
                     help="decode: the decode step only; prefill: the prefill step only "
                          "(profiling runs); both: the full JSON line")
@@ -572,6 +573,9 @@ def main():
     cascade = None
     if not args.no_cascade:
         cascade = _cascade_leg(pa, dev, rank, peaks, flush, stream, args)
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = _fp8_leg(pa, dev, rank, peaks, flush, stream, args, case, runner)
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and args.gpus == 1:
@@ -613,7 +617,36 @@ def main():
         line["mixed"] = mixed
     if cascade is not None:
         line["cascade"] = cascade
+    if fp8 is not None:
+        line["fp8_decode"] = fp8
     print(json.dumps(line), flush=True)
+
+
+def _fp8_leg(pa, dev, rank, peaks, flush, stream, args, case, runner):
+    """The decode workload over an FP8 E4M3 cache (codes of the bf16 cache / 0.02): the
+    bytes actually read (one per element) and the tokens per second against bf16."""
+    kv_scale = 0.02
+    k8 = (case.k_cache.float() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (case.v_cache.float() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    w = case.workload
+    need = pa.pa_decode_workspace_size(len(runner.seqs), w.num_heads, w.num_kv_heads,
+                                       w.head_dim, runner.max_len, runner.window, 0)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(runner.q)
+
+    def step():
+        pa.pa_decode_fp8(runner.q, k8, v8, runner.bt, runner.seq_lens, runner.max_len,
+                         runner.scale, kv_scale, runner.window, 0, key=runner.key,
+                         value=runner.value, slot_mapping=runner.slots, out=out, workspace=ws)
+
+    steps = max(20, args.steps // 10)
+    t = statistics.mean(_time_steps(step, steps, 3, flush, stream))
+    bytes8 = runner.work // 2  # one byte per element instead of two
+    return {"kv_bytes_per_step": bytes8, "ms_per_step": round(t, 5),
+            "gbs": round(bytes8 / (t / 1e3) / 1e9, 2),
+            "frac_of_hbm": round(bytes8 / (t / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "bf16_equivalent_gbs": round(runner.work / (t / 1e3) / 1e9, 2),
+            "kv_scale": kv_scale}
 
 
 def _cascade_leg(pa, dev, rank, peaks, flush, stream, args):
