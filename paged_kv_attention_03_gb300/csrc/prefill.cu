@@ -27,8 +27,9 @@
 //  * One thread issues the MMAs in the order ... P0 V(t-1), S0(t), P1 V(t-1), S1(t) ...,
 //    so each softmax warpgroup works on its tile while the tensor core runs the other
 //    tile's products (ping-pong).
-//  * Warp roles: 0 loads Q and K, 10 loads V, 1 issues MMAs, 2-5 and 6-9 are the two
-//    softmax warpgroups (thread = TMEM lane = accumulator row): mask, online softmax in
+//  * Warp roles: 0-3 and 4-7 are the two softmax warpgroups (200 registers each after
+//    setmaxnreg), 8 loads K, 9 issues MMAs, 10 loads V, 11 loads Q (96 registers); the softmax
+//    warpgroups (thread = TMEM lane = accumulator row): mask, online softmax in
 //    base 2 with the scale folded into the exponent, lazy O rescale (only when the
 //    running max grows by more than 2^8), epilogue.
 //  * Every mbarrier wait is bounded: on timeout the CTA raises an error bit, drains,
@@ -58,8 +59,17 @@ constexpr int BN = 128;                  // keys per KV tile
 constexpr uint32_t HALF = 128u * 128u;   // [128 rows][64 bf16] = 16 KB (one swizzle span)
 constexpr int NSK = 3;                   // K stages
 constexpr int NSV = 2;                   // V stages
-constexpr int kWarpQK = 0, kWarpMma = 1, kWarpV = 10;
-constexpr int kThreads = 11 * 32;
+// Warpgroups 0 and 1 (warps 0-3, 4-7) are the softmax of query tiles 0 and 1 (a warp
+// reaches the TMEM lanes 32 * (warp % 4) ...); warpgroup 2 holds the producers and the
+// MMA issuer.  The producer warpgroup gives up registers so that the
+// softmax threads, which hold a 128-column logit row, get 200.
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpQ = 11;
+constexpr int kThreads = 12 * 32;
+constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 96;
+// Bit (i % 8) set: column pair i of a logit row takes 2^x from the cubic on the FMA pipe.
+constexpr uint32_t kPolyPairs = 0x00u;
+static_assert(kRegsSoftmax * 256 + kRegsProducer * 128 <= 168 * kThreads,
+              "register split exceeds the launch's 168 per thread");
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: S_i at 128 * i, O_i at 256 + 128 * i.
 __host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
@@ -113,7 +123,9 @@ enum : int {
     B_SFULL = B_VEMPTY + NSV,  // [2]: one per query tile
     B_PFULL = B_SFULL + 2,     // [2]
     B_ODONE = B_PFULL + 2,     // [2]
-    NBARS = B_ODONE + 2
+    B_IFULL = B_ODONE + 2,     // [2]: item-info ring slot written
+    B_IEMPTY = B_IFULL + 2,    // [2]: slot read by the MMA issuer and the 8 softmax warps
+    NBARS = B_IEMPTY + 2
 };
 
 template <int HD>
@@ -125,7 +137,8 @@ struct Layout {
     static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
-    static constexpr uint32_t BYTES = OFF_MISC + 16;
+    static constexpr uint32_t OFF_INFO = OFF_MISC + 16;   // item-info ring, 2 x 64 bytes
+    static constexpr uint32_t BYTES = OFF_INFO + 128;
     // At least 116 KB so a single CTA owns an SM (and all of its TMEM).
     static constexpr uint32_t SMEM = (BYTES + 1024 > 118784u ? BYTES + 1024 : 118784u);
 };
@@ -137,6 +150,13 @@ struct Item {
     int seq, kvh, q0, rows0, rows1, q_start, sq, sk, kt0, n_tiles;
     int split;  // shared-prefix mode: key split of the item
 };
+// One slot of the item-info ring; end marks the end of the work list.
+struct alignas(16) ItemSlot {
+    Item it;
+    int end;
+};
+static_assert(sizeof(ItemSlot) == 64, "item-info slots are 64 bytes");
+constexpr int kConsumersPerItem = 9;  // MMA issuer + 8 softmax warps
 
 // PREFIX: the shared-prefix (cascade) mode; item idx = (split, query-tile pair, kv head),
 // the requests play the tokens of one sequence whose keys are the prefix.
@@ -251,6 +271,13 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
     }
 }
 
+// 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -277,6 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sb + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + L::OFF_MISC + 4);
+    // Item-info ring: the Q producer walks the work list once (it skips the items that
+    // have no rows) and hands each valid item to the MMA issuer and the softmax warps, so
+    // their item changes cost no global-memory round trips.
+    ItemSlot *info = reinterpret_cast<ItemSlot *>(sb + L::OFF_INFO);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -300,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_PFULL + i), 4);
             mbar_init(bar(B_ODONE + i), 1);
+            mbar_init(bar(B_IFULL + i), 1);
+            mbar_init(bar(B_IEMPTY + i), kConsumersPerItem);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -327,189 +360,228 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return (blk << p.log2_bs) | (k0 & bs_mask);
     };
-    // One K or V tile (128 keys) of item `it` into shared memory at dst.
+    // One K or V tile (128 keys) of item `it` into shared memory at dst, issued by a whole
+    // warp: each lane issues one box (16-key piece u, 64-dim half h), so the block-table
+    // reads and the box issues overlap instead of queueing behind one thread.
     auto load_kv = [&](const CUtensorMap *map, const Item &it, int key0, uint32_t dst,
                        uint32_t full) {
-#pragma unroll 1
-        for (int u = 0; u < BN / 16; ++u) {
+        static_assert((BN / 16) * NHALF <= 32, "one lane per box");
+        if (lane < (BN / 16) * NHALF) {
+            const int u = lane / NHALF;
+            const int h = lane - u * NHALF;
             const int row = kv_row(it, key0 + u * 16);
-#pragma unroll
-            for (int h = 0; h < NHALF; ++h)
-                tma_load_3d(dst + h * HALF + u * 2048, map, h * 64, it.kvh, row, full);
+            tma_load_3d(dst + h * HALF + u * 2048, map, h * 64, it.kvh, row, full);
         }
     };
 
-    if (warp == kWarpQK) {
-        // ---------------- Q + K producer ----------------
-        if (lane == 0) {
-            prefetch_tmap(&p.tmap_q);
-            prefetch_tmap(&p.tmap_k);
-            uint32_t t = 0, ic = 0;
-            bool ok = true;
-            int idx = blockIdx.x;
-            Item it = get_item<PREFIX>(p, idx, false);
-            while (ok && idx < p.n_items) {
-                if (!it.valid) {
-                    idx += gridDim.x;
-                    if (idx < p.n_items) it = get_item<PREFIX>(p, idx, false);
-                    continue;
-                }
-                // Look ahead to the next valid item and pull its Q into L2.
-                int nidx = idx + gridDim.x;
-                Item nit;
-                nit.valid = false;
-                while (nidx < p.n_items) {
-                    nit = get_item<PREFIX>(p, nidx, false);
-                    if (nit.valid) break;
-                    nidx += gridDim.x;
-                }
-                if (ic >= 1 && !wait1(bar(B_QEMPTY), (ic - 1) & 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
-#pragma unroll
-                for (int h = 0; h < NHALF; ++h) {
-                    tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G, it.q_start + it.q0,
-                                bar(B_QFULL));
-                    if (it.has1)
-                        tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
-                                    it.q_start + it.q0 + T, bar(B_QFULL));
-                }
-                if (nidx < p.n_items && nit.valid) {
+    if (warp >= 8) {
+        // The register limit must be set inside each role's branch: code after a
+        // merge of the two paths would get the smaller of the two limits.
+        setmaxnreg_dec<kRegsProducer>();
+        if (warp == kWarpQ) {
+            // ---------------- Q producer ----------------
+            // Q has a single buffer pair, freed after the item's last S product; K and V
+            // run ahead on their own warps, across item boundaries.
+            if (lane == 0) {
+                prefetch_tmap(&p.tmap_q);
+                uint32_t ic = 0;
+                int idx = blockIdx.x;
+                Item it = get_item<PREFIX>(p, idx, false);
+                while (idx < p.n_items) {
+                    if (!it.valid) {
+                        idx += gridDim.x;
+                        if (idx < p.n_items) it = get_item<PREFIX>(p, idx, false);
+                        continue;
+                    }
+                    // Look ahead to the next valid item and pull its Q into L2.
+                    int nidx = idx + gridDim.x;
+                    Item nit;
+                    nit.valid = false;
+                    while (nidx < p.n_items) {
+                        nit = get_item<PREFIX>(p, nidx, false);
+                        if (nit.valid) break;
+                        nidx += gridDim.x;
+                    }
+                    if (ic >= 2 &&
+                        !wait1(bar(B_IEMPTY + (ic & 1)), ((ic >> 1) - 1) & 1, abort_flag, p.err))
+                        break;
+                    info[ic & 1].it = it;
+                    info[ic & 1].end = 0;
+                    mbar_arrive(bar(B_IFULL + (ic & 1)));
+                    if (ic >= 1 && !wait1(bar(B_QEMPTY), (ic - 1) & 1, abort_flag, p.err)) break;
+                    mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
 #pragma unroll
                     for (int h = 0; h < NHALF; ++h) {
-                        tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G, nit.q_start + nit.q0);
-                        if (nit.has1)
-                            tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
-                                               nit.q_start + nit.q0 + T);
+                        tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G, it.q_start + it.q0,
+                                    bar(B_QFULL));
+                        if (it.has1)
+                            tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                        it.q_start + it.q0 + T, bar(B_QFULL));
                     }
-                }
-                for (int j = 0; j < it.n_tiles; ++j, ++t) {
-                    const int st = t % NSK;
-                    if (t >= NSK &&
-                        !wait1(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
+                    if (nidx < p.n_items && nit.valid) {
+#pragma unroll
+                        for (int h = 0; h < NHALF; ++h) {
+                            tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G, nit.q_start + nit.q0);
+                            if (nit.has1)
+                                tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
+                                                   nit.q_start + nit.q0 + T);
+                        }
                     }
-                    mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
-                    load_kv(&p.tmap_k, it, (it.kt0 + j) * BN, sK + st * L::TILE, bar(B_KFULL + st));
+                    ++ic;
+                    idx = nidx;
+                    it = nit;
                 }
-                ++ic;
-                idx = nidx;
-                it = nit;
+                // End of the list.
+                if (!*abort_flag &&
+                    (ic < 2 ||
+                     wait1(bar(B_IEMPTY + (ic & 1)), ((ic >> 1) - 1) & 1, abort_flag, p.err))) {
+                    info[ic & 1].end = 1;
+                    mbar_arrive(bar(B_IFULL + (ic & 1)));
+                }
             }
-        }
-    } else if (warp == kWarpV) {
-        // ---------------- V producer (also reports per-sequence input errors) ----------------
-        if (lane == 0) {
-            prefetch_tmap(&p.tmap_v);
+        } else if (warp == kWarpK) {
+            // ---------------- K producer (whole warp) ----------------
+            if (lane == 0) prefetch_tmap(&p.tmap_k);
             uint32_t t = 0;
             bool ok = true;
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item<PREFIX>(p, idx, true);
+                const Item it = get_item<PREFIX>(p, idx, false);
+                if (!it.valid) continue;
+                for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                    const int st = t % NSK;
+                    if (t >= NSK &&
+                        !wait_warp(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
+                    __syncwarp();
+                    load_kv(&p.tmap_k, it, (it.kt0 + j) * BN, sK + st * L::TILE, bar(B_KFULL + st));
+                }
+            }
+        } else if (warp == kWarpV) {
+            // ---------------- V producer (whole warp; also reports per-sequence input errors) ----
+            if (lane == 0) prefetch_tmap(&p.tmap_v);
+            uint32_t t = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+                const Item it = get_item<PREFIX>(p, idx, lane == 0);
                 if (!it.valid) continue;
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSV;
                     if (t >= NSV &&
-                        !wait1(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err)) {
+                        !wait_warp(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
+                    __syncwarp();
                     load_kv(&p.tmap_v, it, (it.kt0 + j) * BN, sV + st * L::TILE, bar(B_VFULL + st));
                 }
             }
-        }
-    } else if (warp == kWarpMma) {
-        // ---------------- MMA issuer ----------------
-        // Order on the tensor pipe, across items: P0 V(g-1), S0(g), P1 V(g-1), S1(g).
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
-            uint32_t g = 0;                  // global KV tile counter
-            uint32_t cnt[2] = {0, 0};        // tiles issued per query tile (S / P V)
-            uint32_t ic = 0;                 // items
-            bool ok = true;
-            // Pending P V of the previous KV tile: its V stage, whether it is the first tile
-            // of its item (overwrite O), and whether query tile 1 takes part.
-            bool have_prev = false, prev_first = false, prev_has1 = false;
-            uint32_t prev_g = 0;
-            auto issue_pv = [&](int i, uint32_t gv, bool first) -> bool {
-                const uint32_t c = cnt[i]++;
-                if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err)) return false;
-                if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err))
-                    return false;
-                tc_fence_after();
-                const uint32_t vbase = sV + (gv % NSV) * L::TILE;
-#pragma unroll
-                for (int k = 0; k < KSTEPS_O; ++k) {
-                    const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
-                    mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, b, idesc_o,
-                                (!first || k > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(B_ODONE + i));
-                return true;
-            };
-            auto issue_s = [&](int i, uint32_t gk) {
-                const uint32_t qbase = sQ + i * L::TILE;
-                const uint32_t kbase = sK + (gk % NSK) * L::TILE;
-#pragma unroll
-                for (int k = 0; k < KSTEPS_S; ++k) {
-                    const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                    mma_bf16_ss(tmem + col_s(i), a, b, idesc_s, k > 0);
-                }
-                mma_commit(bar(B_SFULL + i));
-            };
-            // Issue the P V products still pending from the previous KV tile.
-            auto flush = [&]() -> bool {
-                if (!have_prev) return true;
-                have_prev = false;
-                if (!issue_pv(0, prev_g, prev_first)) return false;
-                if (prev_has1 && !issue_pv(1, prev_g, prev_first)) return false;
-                mma_commit(bar(B_VEMPTY + prev_g % NSV));
-                return true;
-            };
-            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item<PREFIX>(p, idx, false);
-                if (!it.valid) continue;
-                // Finish the previous item before waiting for this item's Q, so its
-                // epilogue never waits on a Q load.
-                if (!flush()) break;
-                if (!wait1(bar(B_QFULL), ic & 1, abort_flag, p.err)) break;
-                for (int j = 0; j < it.n_tiles; ++j, ++g) {
-                    const int st = g % NSK;
-                    if (!wait1(bar(B_KFULL + st), (g / NSK) & 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
+        } else if (warp == kWarpMma) {
+            // ---------------- MMA issuer ----------------
+            // Order on the tensor pipe, across items: P0 V(g-1), S0(g), P1 V(g-1), S1(g).
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+                constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
+                uint32_t g = 0;                  // global KV tile counter
+                uint32_t cnt[2] = {0, 0};        // tiles issued per query tile (S / P V)
+                uint32_t ic = 0;                 // items
+                bool ok = true;
+                // Pending P V of the previous KV tile: its V stage, whether it is the first tile
+                // of its item (overwrite O), and whether query tile 1 takes part.
+                bool have_prev = false, prev_first = false, prev_has1 = false;
+                uint32_t prev_g = 0;
+                auto issue_pv = [&](int i, uint32_t gv, bool first) -> bool {
+                    const uint32_t c = cnt[i]++;
+                    if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err)) return false;
+                    if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err))
+                        return false;
                     tc_fence_after();
-                    // query tile 0
-                    if (have_prev && !issue_pv(0, prev_g, prev_first)) {
+                    const uint32_t vbase = sV + (gv % NSV) * L::TILE;
+    #pragma unroll
+                    for (int k = 0; k < KSTEPS_O; ++k) {
+                        const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
+                        mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, b, idesc_o,
+                                    (!first || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_ODONE + i));
+                    return true;
+                };
+                auto issue_s = [&](int i, uint32_t gk) {
+                    const uint32_t qbase = sQ + i * L::TILE;
+                    const uint32_t kbase = sK + (gk % NSK) * L::TILE;
+    #pragma unroll
+                    for (int k = 0; k < KSTEPS_S; ++k) {
+                        const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
+                        const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
+                        mma_bf16_ss(tmem + col_s(i), a, b, idesc_s, k > 0);
+                    }
+                    mma_commit(bar(B_SFULL + i));
+                };
+                // Issue the P V products still pending from the previous KV tile.
+                auto flush = [&]() -> bool {
+                    if (!have_prev) return true;
+                    have_prev = false;
+                    if (!issue_pv(0, prev_g, prev_first)) return false;
+                    if (prev_has1 && !issue_pv(1, prev_g, prev_first)) return false;
+                    mma_commit(bar(B_VEMPTY + prev_g % NSV));
+                    return true;
+                };
+                for (;; ++ic) {
+                    if (!wait1(bar(B_IFULL + (ic & 1)), (ic >> 1) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    issue_s(0, g);
-                    // query tile 1
-                    if (have_prev && prev_has1 && !issue_pv(1, prev_g, prev_first)) {
+                    const Item it = info[ic & 1].it;
+                    const bool end = info[ic & 1].end != 0;
+                    mbar_arrive(bar(B_IEMPTY + (ic & 1)));
+                    if (end) break;
+                    // Finish the previous item before waiting for this item's Q, so its
+                    // epilogue never waits on a Q load.
+                    if (!flush() || !wait1(bar(B_QFULL), ic & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    if (have_prev) mma_commit(bar(B_VEMPTY + prev_g % NSV));
-                    if (it.has1) issue_s(1, g);
-                    mma_commit(bar(B_KEMPTY + st));
-                    if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY));
-                    have_prev = true;
-                    prev_g = g;
-                    prev_first = j == 0;
-                    prev_has1 = it.has1;
+                    for (int j = 0; j < it.n_tiles; ++j, ++g) {
+                        const int st = g % NSK;
+                        // query tile 0: P0 V of the previous tile needs no K, so it goes to
+                        // the tensor core before the wait for K(g)
+                        if (have_prev && !issue_pv(0, prev_g, prev_first)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!wait1(bar(B_KFULL + st), (g / NSK) & 1, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(0, g);
+                        // query tile 1
+                        if (have_prev && prev_has1 && !issue_pv(1, prev_g, prev_first)) {
+                            ok = false;
+                            break;
+                        }
+                        if (have_prev) mma_commit(bar(B_VEMPTY + prev_g % NSV));
+                        if (it.has1) issue_s(1, g);
+                        mma_commit(bar(B_KEMPTY + st));
+                        if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY));
+                        have_prev = true;
+                        prev_g = g;
+                        prev_first = j == 0;
+                        prev_has1 = it.has1;
+                    }
+                    if (!ok) break;
                 }
-                ++ic;
+                if (ok) flush();
             }
-            if (ok) flush();
         }
-    } else if (warp >= 2 && warp < 10) {
-        // ---------------- softmax warpgroups (warps 2..5: tile 0, 6..9: tile 1) ----------------
-        const int wg = (warp - 2) >> 2;
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        // ---------------- softmax warpgroups (warps 0..3: tile 0, 4..7: tile 1) ----------------
+        const int wg = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -523,9 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gt = 0;   // global KV tile counter
         uint32_t c = 0;    // tiles this warpgroup has processed
         bool ok = true;
-        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-            const Item it = get_item<PREFIX>(p, idx, false);
-            if (!it.valid) continue;
+        for (uint32_t ic = 0; ok; ++ic) {
+            if (!wait_warp(bar(B_IFULL + (ic & 1)), (ic >> 1) & 1, abort_flag, p.err)) break;
+            const Item it = info[ic & 1].it;
+            const bool end = info[ic & 1].end != 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_IEMPTY + (ic & 1)));
+            if (end) break;
             if (wg == 1 && !it.has1) {
                 gt += it.n_tiles;
                 continue;
@@ -559,15 +635,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *s = &sc[0][0];
 
                 const int key0 = (it.kt0 + j) * BN;
-                const bool all_visible = key0 + BN - 1 <= pos && key0 >= lo;
                 // Row maximum as 8 independent 3-input max chains, then a tree (a single
                 // dependent chain of 128 maxima would cost ~4 cycles per element).
-                if (!all_visible) {
+                // Edge tiles: the causal bound and the window's lower bound are masked
+                // separately, so a diagonal tile pays for one compare per element.
+                if (key0 + BN - 1 > pos) {
+                    const int last = pos - key0;  // columns past it lie in the future
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) {
-                        const int k = key0 + i;
-                        if (k > pos || k < lo) s[i] = -INFINITY;
-                    }
+                    for (int i = 0; i < BN; ++i)
+                        if (i > last) s[i] = -INFINITY;
+                }
+                if (key0 < lo) {
+                    const int first = lo - key0;  // columns before it lie outside the window
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (i < first) s[i] = -INFINITY;
                 }
                 static_assert(BN == 128, "the max tree covers 128 columns");
                 float mx8[8];  // mx8[a] = max over s[a + 8k], k = 0..15
@@ -609,20 +691,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // P = 2^(s * scale_log2 - m) as bf16 over the low 64 columns of S; the
                 // denominator sums the bf16 weights the MMA actually uses.
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+                // Pairs of columns go through packed f32x2 arithmetic; the pairs picked by
+                // kPolyPairs take 2^x on the FMA pipe, the rest on the MUFU unit, which
+                // would otherwise bound the tile.
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc[2] = {0ull, 0ull};  // packed partial sums of the bf16 weights
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2_approx(fmaf(s[cc * 64 + 2 * i], sl2, -m_use));
-                        const float e1 = ex2_approx(fmaf(s[cc * 64 + 2 * i + 1], sl2, -m_use));
+                        const uint64_t x = f2_fma(f2_pack(s[cc * 64 + 2 * i], s[cc * 64 + 2 * i + 1]),
+                                                  sl2x2, negm2);
+                        float e0, e1;
+                        if ((kPolyPairs >> (i & 7)) & 1u) {
+                            exp2_fma_x2(x, e0, e1);
+                        } else {
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            e0 = ex2_approx(x0);
+                            e1 = ex2_approx(x1);
+                        }
                         pk[i] = pack_bf16x2(e0, e1);
-                        ls[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                        acc[i & 1] = f2_add(acc[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                                __uint_as_float(pk[i] & 0xffff0000u)));
                     }
                     tmem_st_32x32b_x32_u(scol + cc * 32, pk);
                 }
-                l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc[0], a0, a1);
+                    f2_unpack(acc[1], b0, b1);
+                    l_sum += (a0 + a1) + (b0 + b1);
+                }
                 // Keys of the sequence's last, partly filled 16-key piece that lie past sk
                 // are stale cache rows: warpgroup 0 zeroes them in the V tile (before
                 // either P V of this tile is issued) so 0 * V stays 0.
@@ -685,21 +787,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(it.q_start + it.q0 + tok) *
                                               p.num_heads + it.kvh * G + g) * HD;
+            // A row is one thread's: 32-byte stores write whole sectors (16-byte ones leave
+            // the L2 half-sector writes); the output is 32-byte aligned in practice.
+            const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll 1
             for (int cc = 0; cc < HD / 32; ++cc) {
                 float o[32];
                 tmem_ld_32x32b_x32(ocol + cc * 32, o);
                 tmem_wait_ld_regs(o);
                 if (valid) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+                    uint32_t w[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 v;
-                        v.x = pack_bf16x2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
-                        v.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-                        v.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-                        v.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-                        d4[i] = v;
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(o[2 * i] * inv, o[2 * i + 1] * inv);
+                    if (v8) {
+                        st_global_v8(dst + cc * 32, w);
+                        st_global_v8(dst + cc * 32 + 16, w + 8);
+                    } else {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
                 }
             }

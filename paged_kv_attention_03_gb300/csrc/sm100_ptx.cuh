@@ -326,6 +326,19 @@ __device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t mask) {
 namespace pa {
 namespace sm100 {
 
+// ------------------------------------------------------ register budget ---
+// Raise / lower this warpgroup's per-thread register limit.  Every thread of the
+// warpgroup executes the same instruction; the increases of a block must be covered by
+// its decreases (the registers the block was launched with are the whole pool).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------- packed fp32 (f32x2) ---
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
     uint64_t r;
