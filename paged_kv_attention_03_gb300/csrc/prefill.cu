@@ -790,6 +790,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A row is one thread's: 32-byte stores write whole sectors (16-byte ones leave
             // the L2 half-sector writes); the output is 32-byte aligned in practice.
             const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+            if (HD == 128 && v8 && (G & 3) == 0) {
+                // The 4 rows of a lane quad are 4 consecutive heads of one token: 1 KB of
+                // contiguous output.  Two xor-shuffle rounds give lane j of the quad the
+                // j-th 32-byte slice (of each 128-column half) of all 4 rows, so every
+                // store instruction writes whole 128-byte lines, 4 lanes per line.
+                const int j = lane & 3;
+                const bool b0 = (j & 1) != 0, b1 = (j & 2) != 0;
+                __nv_bfloat16 *qdst = dst - j * HD;  // the quad's first row
+#pragma unroll 1
+                for (int t = 0; t < 2; ++t) {
+                    float o[2][32];
+                    tmem_ld_32x32b_x32(ocol + t * 64, o[0]);
+                    tmem_ld_32x32b_x32(ocol + t * 64 + 32, o[1]);
+                    tmem_wait_ld_regs(o[0]);
+                    tmem_wait_ld_regs(o[1]);
+                    // a[c][k]: word k of 32-byte slice c (columns 64t + 16c ...) of my row
+                    uint32_t a[4][8];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            a[c][k] = pack_bf16x2(o[c >> 1][(c & 1) * 16 + 2 * k] * inv,
+                                                  o[c >> 1][(c & 1) * 16 + 2 * k + 1] * inv);
+                    // Round 1 (partner j ^ 2): bb[r1][b] = (row (j & 1) | 2 r1, slice (j & 2) | b)
+                    uint32_t bb[2][2][8];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t send = b1 ? a[b][k] : a[2 | b][k];
+                            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+                            bb[0][b][k] = b1 ? recv : a[b][k];
+                            bb[1][b][k] = b1 ? a[2 | b][k] : recv;
+                        }
+                    // Round 2 (partner j ^ 1): f[r] = (row r, slice j)
+                    uint32_t f[4][8];
+#pragma unroll
+                    for (int r1 = 0; r1 < 2; ++r1)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t send = b0 ? bb[r1][0][k] : bb[r1][1][k];
+                            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            f[2 * r1][k] = b0 ? recv : bb[r1][0][k];
+                            f[2 * r1 + 1][k] = b0 ? bb[r1][1][k] : recv;
+                        }
+                    if (valid) {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) st_global_v8(qdst + r * HD + (j + 4 * t) * 16, f[r]);
+                    }
+                }
+                tc_fence_before();
+                continue;
+            }
 #pragma unroll 1
             for (int cc = 0; cc < HD / 32; ++cc) {
                 float o[32];
