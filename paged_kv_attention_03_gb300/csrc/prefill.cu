@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // would otherwise bound the tile.
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_use, -m_use);
-                uint64_t acc[2] = {0ull, 0ull};  // packed partial sums of the bf16 weights
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums of the bf16 weights
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t pk[32];
@@ -714,17 +714,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             e1 = ex2_approx(x1);
                         }
                         pk[i] = pack_bf16x2(e0, e1);
-                        acc[i & 1] = f2_add(acc[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                                __uint_as_float(pk[i] & 0xffff0000u)));
+                        add_bf16x2_f32(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], pk[i]);
                     }
                     tmem_st_32x32b_x32_u(scol + cc * 32, pk);
                 }
-                {
-                    float a0, a1, b0, b1;
-                    f2_unpack(acc[0], a0, a1);
-                    f2_unpack(acc[1], b0, b1);
-                    l_sum += (a0 + a1) + (b0 + b1);
-                }
+                l_sum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
                 // Keys of the sequence's last, partly filled 16-key piece that lie past sk
                 // are stale cache rows: warpgroup 0 zeroes them in the V tile (before
                 // either P V of this tile is issued) so 0 * V stays 0.

@@ -358,6 +358,18 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// lo += float(bf16 low half of v), hi += float(bf16 high half of v): the mixed-precision
+// add takes the bf16 halves directly (bf16 -> f32 is exact, the add rounds to nearest).
+__device__ __forceinline__ void add_bf16x2_f32(float &lo, float &hi, uint32_t v) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %2;\n"
+        "add.rn.f32.bf16 %0, l, %0;\n"
+        "add.rn.f32.bf16 %1, h, %1;\n"
+        "}\n"
+        : "+f"(lo), "+f"(hi)
+        : "r"(v));
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
