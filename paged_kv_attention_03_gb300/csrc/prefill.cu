@@ -14,8 +14,10 @@
 //    T = floor(128 / G) consecutive tokens (row m = token m / G, head m % G).  A work
 //    item is two consecutive query tiles (2T tokens) of one (sequence, kv head), so every
 //    K/V tile fetched feeds 256 rows: half the K/V bytes per FLOP of one tile.
-//  * Persistent CTAs, one per SM, walk the items round-robin, longest first; the next
-//    item's Q is prefetched into L2 while the current one runs.
+//  * Persistent CTAs, one per SM.  The work list is ordered longest first and its valid
+//    items are dealt to the CTAs in snake order; each CTA's scheduler warp publishes its
+//    items to the other roles through a shared-memory ring.  The next item's Q is
+//    prefetched into L2 while the current one runs.
 //  * K/V come straight from the paged cache: the TMA producers walk block_table and
 //    fetch each 16-key piece of a page as one 3-D box {64 dims, 1 kv head, 16 rows}
 //    with 128-byte swizzle; pieces past the sequence come from an out-of-range
@@ -28,7 +30,8 @@
 //    so each softmax warpgroup works on its tile while the tensor core runs the other
 //    tile's products (ping-pong).
 //  * Warp roles: 0-3 and 4-7 are the two softmax warpgroups (200 registers each after
-//    setmaxnreg), 8 loads K, 9 issues MMAs, 10 loads V, 11 loads Q (96 registers); the softmax
+//    setmaxnreg), 8 loads K, 9 issues MMAs, 10 loads V, 11 schedules the CTA's items and
+//    loads Q (96 registers); the softmax
 //    warpgroups (thread = TMEM lane = accumulator row): mask, online softmax in
 //    base 2 with the scale folded into the exponent, lazy O rescale (only when the
 //    running max grows by more than 2^8), epilogue.
@@ -63,7 +66,9 @@ constexpr int NSV = 2;                   // V stages
 // reaches the TMEM lanes 32 * (warp % 4) ...); warpgroup 2 holds the producers and the
 // MMA issuer.  The producer warpgroup gives up registers so that the
 // softmax threads, which hold a 128-column logit row, get 200.
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpQ = 11;
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpSched = 11;
+constexpr uint32_t kRing = 8;   // item-info ring slots
+constexpr uint32_t kAhead = 6;  // items published beyond the last Q load
 constexpr int kThreads = 12 * 32;
 constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 96;
 // Bit (i % 8) set: column pair i of a logit row takes 2^x from the cubic on the FMA pipe.
@@ -123,9 +128,9 @@ enum : int {
     B_SFULL = B_VEMPTY + NSV,  // [2]: one per query tile
     B_PFULL = B_SFULL + 2,     // [2]
     B_ODONE = B_PFULL + 2,     // [2]
-    B_IFULL = B_ODONE + 2,     // [2]: item-info ring slot written
-    B_IEMPTY = B_IFULL + 2,    // [2]: slot read by the MMA issuer and the 8 softmax warps
-    NBARS = B_IEMPTY + 2
+    B_IFULL = B_ODONE + 2,       // [kRing]: item-info ring slot written
+    B_IEMPTY = B_IFULL + kRing,  // [kRing]: slot read by every consumer
+    NBARS = B_IEMPTY + kRing
 };
 
 template <int HD>
@@ -137,8 +142,8 @@ struct Layout {
     static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
-    static constexpr uint32_t OFF_INFO = OFF_MISC + 16;   // item-info ring, 2 x 64 bytes
-    static constexpr uint32_t BYTES = OFF_INFO + 128;
+    static constexpr uint32_t OFF_INFO = OFF_MISC + 16;   // item-info ring, kRing x 64 bytes
+    static constexpr uint32_t BYTES = OFF_INFO + kRing * 64;
     // At least 116 KB so a single CTA owns an SM (and all of its TMEM).
     static constexpr uint32_t SMEM = (BYTES + 1024 > 118784u ? BYTES + 1024 : 118784u);
 };
@@ -156,7 +161,7 @@ struct alignas(16) ItemSlot {
     int end;
 };
 static_assert(sizeof(ItemSlot) == 64, "item-info slots are 64 bytes");
-constexpr int kConsumersPerItem = 9;  // MMA issuer + 8 softmax warps
+constexpr int kConsumersPerItem = 11;  // K and V producers, MMA issuer, 8 softmax warps
 
 // PREFIX: the shared-prefix (cascade) mode; item idx = (split, query-tile pair, kv head),
 // the requests play the tokens of one sequence whose keys are the prefix.
@@ -304,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sb + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + L::OFF_MISC + 4);
-    // Item-info ring: the Q producer walks the work list once (it skips the items that
-    // have no rows) and hands each valid item to the MMA issuer and the softmax warps, so
-    // their item changes cost no global-memory round trips.
+    // Item-info ring: the scheduler warp picks this CTA's items and hands each one to
+    // every other role, so no role walks the work list or pays a global-memory round
+    // trip when it changes item.
     ItemSlot *info = reinterpret_cast<ItemSlot *>(sb + L::OFF_INFO);
 
     const int warp = threadIdx.x >> 5;
@@ -331,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_PFULL + i), 4);
             mbar_init(bar(B_ODONE + i), 1);
+        }
+        for (uint32_t i = 0; i < kRing; ++i) {
             mbar_init(bar(B_IFULL + i), 1);
             mbar_init(bar(B_IEMPTY + i), kConsumersPerItem);
         }
@@ -378,75 +385,147 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The register limit must be set inside each role's branch: code after a
         // merge of the two paths would get the smaller of the two limits.
         setmaxnreg_dec<kRegsProducer>();
-        if (warp == kWarpQ) {
-            // ---------------- Q producer ----------------
-            // Q has a single buffer pair, freed after the item's last S product; K and V
-            // run ahead on their own warps, across item boundaries.
-            if (lane == 0) {
-                prefetch_tmap(&p.tmap_q);
-                uint32_t ic = 0;
-                int idx = blockIdx.x;
-                Item it = get_item<PREFIX>(p, idx, false);
-                while (idx < p.n_items) {
-                    if (!it.valid) {
-                        idx += gridDim.x;
-                        if (idx < p.n_items) it = get_item<PREFIX>(p, idx, false);
+        // Take ring slot ic (every consumer): false at the end of the list or on abort.
+        auto take_item = [&](uint32_t ic, Item &it) -> bool {
+            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err))
+                return false;
+            it = info[ic % kRing].it;
+            const bool end = info[ic % kRing].end != 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_IEMPTY + ic % kRing));
+            return !end;
+        };
+        if (warp == kWarpSched) {
+            // ---------------- scheduler + Q producer (whole warp) ----------------
+            // The work list is ordered longest first.  Its valid items (those with query
+            // rows) are dealt to the CTAs in snake order: rank v goes to CTA v mod P in
+            // even rounds and to CTA P - 1 - (v mod P) in odd ones, which evens out the
+            // CTAs' total work.  The warp scans 32 list positions per step; every CTA
+            // scans the whole list, and position i reports its input errors only in CTA
+            // i mod P.  Items are published up to kAhead beyond the last Q load, so the K
+            // and V producers can run ahead across short items.
+            if (lane == 0) prefetch_tmap(&p.tmap_q);
+            const uint32_t P = gridDim.x, cta = blockIdx.x;
+            const int Hkv = p.num_kv_heads;
+            const int n_pairs = p.n_items / Hkv;  // (query block, sequence) pairs
+            // Target slot of round r: the snake order.
+            auto target = [&](uint32_t r) -> uint32_t { return r * P + ((r & 1u) ? P - 1u - cta : cta); };
+            uint32_t pub = 0, loaded = 0;  // items published / whose Q is loaded
+            uint32_t vrank = 0;            // valid items in the scanned part of the list
+            int scan = 0, win = 0;         // next pair to scan; first pair of the window
+            uint32_t mine = 0;             // window pairs holding items of this CTA
+            uint32_t r0_lane = 0;          // this lane's pair: rank of its first item
+            int cur = -1;                  // pair being enumerated (window lane), or -1
+            uint32_t cur_r0 = 0, cur_round = 0;
+            bool ok = true;
+            // One step per iteration, so a Q load (which gates the item's first S product)
+            // never waits behind a scan: load Q when its buffer is free, else scan one
+            // window or publish one item, else wait for the Q buffer.
+            for (;;) {
+                if (loaded < pub) {
+                    bool ready = true;
+                    if (lane == 0 && loaded >= 1) ready = mbar_test_wait(bar(B_QEMPTY), (loaded - 1) & 1);
+                    if (__shfl_sync(0xffffffffu, ready, 0)) {
+                        if (lane == 0) {
+                            // The slot is intact: pub <= loaded + kAhead < loaded + kRing.
+                            const Item it = info[loaded % kRing].it;
+                            mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
+#pragma unroll
+                            for (int h = 0; h < NHALF; ++h) {
+                                tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                            it.q_start + it.q0, bar(B_QFULL));
+                                if (it.has1)
+                                    tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64,
+                                                it.kvh * G, it.q_start + it.q0 + T, bar(B_QFULL));
+                            }
+                            if (loaded + 1 < pub) {  // pull the next item's Q into L2
+                                const Item nit = info[(loaded + 1) % kRing].it;
+#pragma unroll
+                                for (int h = 0; h < NHALF; ++h) {
+                                    tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
+                                                       nit.q_start + nit.q0);
+                                    if (nit.has1)
+                                        tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
+                                                           nit.q_start + nit.q0 + T);
+                                }
+                            }
+                        }
+                        ++loaded;
                         continue;
                     }
-                    // Look ahead to the next valid item and pull its Q into L2.
-                    int nidx = idx + gridDim.x;
-                    Item nit;
-                    nit.valid = false;
-                    while (nidx < p.n_items) {
-                        nit = get_item<PREFIX>(p, nidx, false);
-                        if (nit.valid) break;
-                        nidx += gridDim.x;
+                }
+                if (pub < loaded + kAhead && (cur >= 0 || mine != 0 || scan < n_pairs)) {
+                    if (cur < 0 && mine == 0) {
+                        // Scan 32 pairs: the kv heads of a pair are all valid or none.
+                        const int pp = scan + lane;
+                        const bool v = pp < n_pairs &&
+                                       get_item<PREFIX>(p, pp * Hkv,
+                                                        static_cast<uint32_t>(pp) % P == cta).valid;
+                        const uint32_t vm = __ballot_sync(0xffffffffu, v);
+                        r0_lane = vrank + static_cast<uint32_t>(Hkv) * __popc(vm & ((1u << lane) - 1u));
+                        // Does one of this CTA's ranks fall in [r0, r0 + Hkv)?  Only the
+                        // first two rounds from r0 / P can hold the first one.
+                        bool own = false;
+                        if (v) {
+                            const uint32_t r = r0_lane / P;
+                            const uint32_t t0 = target(r), t1 = target(r + 1);
+                            own = (t0 >= r0_lane && t0 < r0_lane + Hkv) || t1 < r0_lane + Hkv;
+                        }
+                        mine = __ballot_sync(0xffffffffu, own);
+                        win = scan;
+                        scan += 32;
+                        vrank += static_cast<uint32_t>(Hkv) * __popc(vm);
+                        continue;
                     }
-                    if (ic >= 2 &&
-                        !wait1(bar(B_IEMPTY + (ic & 1)), ((ic >> 1) - 1) & 1, abort_flag, p.err))
-                        break;
-                    info[ic & 1].it = it;
-                    info[ic & 1].end = 0;
-                    mbar_arrive(bar(B_IFULL + (ic & 1)));
-                    if (ic >= 1 && !wait1(bar(B_QEMPTY), (ic - 1) & 1, abort_flag, p.err)) break;
-                    mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
-#pragma unroll
-                    for (int h = 0; h < NHALF; ++h) {
-                        tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G, it.q_start + it.q0,
-                                    bar(B_QFULL));
-                        if (it.has1)
-                            tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
-                                        it.q_start + it.q0 + T, bar(B_QFULL));
+                    if (cur < 0) {
+                        cur = __ffs(mine) - 1;
+                        mine &= mine - 1u;
+                        cur_r0 = __shfl_sync(0xffffffffu, r0_lane, cur);
+                        cur_round = cur_r0 / P;
                     }
-                    if (nidx < p.n_items && nit.valid) {
-#pragma unroll
-                        for (int h = 0; h < NHALF; ++h) {
-                            tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G, nit.q_start + nit.q0);
-                            if (nit.has1)
-                                tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
-                                                   nit.q_start + nit.q0 + T);
+                    const uint32_t tv = target(cur_round++);
+                    if (tv < cur_r0) continue;
+                    if (tv >= cur_r0 + Hkv) {
+                        cur = -1;
+                        continue;
+                    }
+                    const int idx = (win + cur) * Hkv + static_cast<int>(tv - cur_r0);
+                    if (lane == 0) {
+                        const Item it = get_item<PREFIX>(p, idx, false);
+                        if (pub >= kRing && !wait1(bar(B_IEMPTY + pub % kRing),
+                                                   ((pub / kRing) - 1) & 1, abort_flag, p.err)) {
+                            ok = false;
+                        } else {
+                            info[pub % kRing].it = it;
+                            info[pub % kRing].end = 0;
+                            mbar_arrive(bar(B_IFULL + pub % kRing));
                         }
                     }
-                    ++ic;
-                    idx = nidx;
-                    it = nit;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    ++pub;
+                    continue;
                 }
-                // End of the list.
-                if (!*abort_flag &&
-                    (ic < 2 ||
-                     wait1(bar(B_IEMPTY + (ic & 1)), ((ic >> 1) - 1) & 1, abort_flag, p.err))) {
-                    info[ic & 1].end = 1;
-                    mbar_arrive(bar(B_IFULL + (ic & 1)));
-                }
+                if (loaded == pub) break;  // the list is exhausted and every Q loaded
+                // Only a Q load can make progress: wait for its buffer.
+                if (lane == 0) ok = wait1(bar(B_QEMPTY), (loaded - 1) & 1, abort_flag, p.err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            // End of the list.
+            if (ok && lane == 0 && !*abort_flag &&
+                (pub < kRing ||
+                 wait1(bar(B_IEMPTY + pub % kRing), ((pub / kRing) - 1) & 1, abort_flag, p.err))) {
+                info[pub % kRing].end = 1;
+                mbar_arrive(bar(B_IFULL + pub % kRing));
             }
         } else if (warp == kWarpK) {
             // ---------------- K producer (whole warp) ----------------
             if (lane == 0) prefetch_tmap(&p.tmap_k);
             uint32_t t = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item<PREFIX>(p, idx, false);
-                if (!it.valid) continue;
+            Item it;
+            for (uint32_t ic = 0; ok && take_item(ic, it); ++ic) {
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSK;
                     if (t >= NSK &&
@@ -460,13 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == kWarpV) {
-            // ---------------- V producer (whole warp; also reports per-sequence input errors) ----
+            // ---------------- V producer (whole warp) ----------------
             if (lane == 0) prefetch_tmap(&p.tmap_v);
             uint32_t t = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
-                const Item it = get_item<PREFIX>(p, idx, lane == 0);
-                if (!it.valid) continue;
+            Item it;
+            for (uint32_t ic = 0; ok && take_item(ic, it); ++ic) {
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSV;
                     if (t >= NSV &&
@@ -531,13 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 for (;; ++ic) {
-                    if (!wait1(bar(B_IFULL + (ic & 1)), (ic >> 1) & 1, abort_flag, p.err)) {
+                    if (!wait1(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const Item it = info[ic & 1].it;
-                    const bool end = info[ic & 1].end != 0;
-                    mbar_arrive(bar(B_IEMPTY + (ic & 1)));
+                    const Item it = info[ic % kRing].it;
+                    const bool end = info[ic % kRing].end != 0;
+                    mbar_arrive(bar(B_IEMPTY + ic % kRing));
                     if (end) break;
                     // Finish the previous item before waiting for this item's Q, so its
                     // epilogue never waits on a Q load.
@@ -596,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t c = 0;    // tiles this warpgroup has processed
         bool ok = true;
         for (uint32_t ic = 0; ok; ++ic) {
-            if (!wait_warp(bar(B_IFULL + (ic & 1)), (ic >> 1) & 1, abort_flag, p.err)) break;
-            const Item it = info[ic & 1].it;
-            const bool end = info[ic & 1].end != 0;
+            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err)) break;
+            const Item it = info[ic % kRing].it;
+            const bool end = info[ic % kRing].end != 0;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_IEMPTY + (ic & 1)));
+            if (lane == 0) mbar_arrive(bar(B_IEMPTY + ic % kRing));
             if (end) break;
             if (wg == 1 && !it.has1) {
                 gt += it.n_tiles;
