@@ -503,6 +503,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const Deco
         __syncwarp();
     }
     cp_async_wait<0>();
+    // The combine kernel may start launching now (it waits for this grid to finish).
+    sm100::griddep_launch_dependents();
 
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -571,6 +573,7 @@ template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelParams p,
                                                              int batch) {
     constexpr int PER_LANE = D / 32;
+    sm100::griddep_wait();  // launched early (programmatic serialization): the splits must be done
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int b = gw / p.num_heads;
@@ -666,8 +669,21 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
     e = cudaGetLastError();
     if (e != cudaSuccess || (plan.num_splits == 1 && kp.st_o == nullptr)) return e;
+    // Programmatic stream serialization: the combine grid launches while the last split
+    // CTAs finish, and waits for them on the device.
     const int warps = batch * kp.num_heads;
-    decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(kp, batch);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((warps + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, kp, batch);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -341,6 +341,15 @@ __device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t mask) {
 namespace pa {
 namespace sm100 {
 
+// ------------------------------------------------- programmatic dependent launch ---
+// Let the next kernel of the stream (launched with programmatic stream serialization)
+// start launching; it still waits for this grid's completion in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid of the stream has completed and its memory is visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------ register budget ---
 // Raise / lower this warpgroup's per-thread register limit.  Every thread of the
 // warpgroup executes the same instruction; the increases of a block must be covered by
