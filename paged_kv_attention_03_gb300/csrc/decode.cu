@@ -35,6 +35,11 @@ namespace pa {
 
 namespace {
 
+// Resident split CTAs per SM: 4 warps with a 2-stage ring each (64 KB of shared memory
+// at head_dim 128) and at most 168 registers a thread, so three fit.  More resident CTAs
+// hide the pipeline fill at each CTA's start behind the other CTAs' streaming.
+constexpr int kDecodeCtasPerSm = 3;
+
 using sm100::ex2_approx;
 
 struct DecodeKernelParams {
@@ -126,7 +131,7 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // FP8: the cache holds E4M3 codes (x / kv_scale); tiles are converted to bf16 in shared
 // memory after they land, and kv_scale is applied to the scores (K) and results (V).
 template <int D, int NWARPS, int NSTAGES, bool FP8>
-__global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const DecodeKernelParams p) {
+__global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
 }
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 3;
+constexpr int kDecodeStages = 2;
 
 template <int D>
 constexpr int decode_smem_bytes() {
@@ -707,10 +712,10 @@ bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int m
     } else if (num_splits_request > 0) {
         splits = num_splits_request;
     } else {
-        // Enough CTAs for ~16 per SM over the run (load balance across ragged
-        // lengths), but no split shorter than 256 keys (4 units per warp).
+        // Enough CTAs for ~12 per SM over the run (4 per resident slot: load balance
+        // across ragged lengths), but no split shorter than 256 keys (4 units per warp).
         const int64_t units = static_cast<int64_t>(batch) * num_kv_heads * p.head_tiles;
-        const int64_t target = 16LL * 152;
+        const int64_t target = 12LL * 152;
         int64_t s = (target + units - 1) / units;
         const int64_t by_len = (span + 255) / 256;
         if (s > by_len) s = by_len;
