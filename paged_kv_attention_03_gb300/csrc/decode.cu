@@ -111,13 +111,48 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-// Two FP8 E4M3 codes (low byte first) -> bf16x2, exactly: every E4M3 value (at most 4
-// significant bits, exponents 2^-9 .. 2^8) is an f16 and a bf16.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+// Two FP8 E4M3 codes (low byte first) -> f16x2, exactly: every E4M3 value (at most 4
+// significant bits, exponents 2^-9 .. 2^8) is an f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     uint32_t h;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    return pack_bf16x2(f.x, f.y);
+    return h;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// acc += float(f16 low half of v) + float(f16 high half of v) (mixed-precision adds).
+__device__ __forceinline__ void add_f16x2_f32(float &acc, uint32_t v) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %1;\n"
+        "add.rn.f32.f16 %0, l, %0;\n"
+        "add.rn.f32.f16 %0, h, %0;\n"
+        "}\n"
+        : "+f"(acc)
+        : "r"(v));
+}
+
+// D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Swizzled 16-byte chunk of an fp8 tile row (D bytes): the 8 rows an ldmatrix reads
+// land in 8 different bank groups.
+template <int D>
+__device__ __forceinline__ int swz8(int c, int r) {
+    if constexpr (D >= 128) return c ^ (r & 7);
+    else return c ^ ((r >> 1) & 3);
 }
 
 // Two fp32 values -> two FP8 E4M3 codes (lo in the low byte): round to nearest even,
@@ -128,8 +163,11 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// FP8: the cache holds E4M3 codes (x / kv_scale); tiles are converted to bf16 in shared
-// memory after they land, and kv_scale is applied to the scores (K) and results (V).
+// FP8: the cache holds E4M3 codes (x / kv_scale).  The products run as f16 MMAs on the
+// codes converted in registers (one cvt per pair): K fragments come from ldmatrix on the
+// fp8 rows with the head-dim index permuted alike in Q, V fragments from a transposing
+// ldmatrix on byte pairs plus one byte permute (even and odd head dims in separate
+// MMAs).  kv_scale is applied to the scores (K) and the results (V); Q and P are f16.
 template <int D, int NWARPS, int NSTAGES, bool FP8>
 __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
@@ -140,14 +178,15 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     constexpr int PASSES = 16 / ROWS_PER_PASS;
     constexpr int KSTEPS = D / 16;
     constexpr int DTILES = D / 8;
-    // FP8 ring: 16-key tiles of D bytes per row; then one bf16 K + V tile per warp.
+    // FP8 ring: 16-key tiles of D bytes per row, twice as many stages in the same space.
     constexpr int TILE8 = 16 * D;
     constexpr int STAGE8 = 2 * TILE8;
     constexpr int CPR8 = D / 16;  // 16-byte chunks per fp8 row
     constexpr int RPP8 = 32 / CPR8;
     constexpr int PASSES8 = 16 / RPP8;
-    static_assert(!FP8 || NSTAGES * STAGE8 + STAGE_BYTES <= NSTAGES * STAGE_BYTES,
-                  "fp8 ring + conversion tile fit the per-warp share");
+    constexpr int NST = FP8 ? 2 * NSTAGES : NSTAGES;  // ring depth
+    constexpr int SB = FP8 ? STAGE8 : STAGE_BYTES;     // bytes per stage
+    static_assert(NST * SB <= NSTAGES * STAGE_BYTES, "the ring fits the per-warp share");
 
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -245,13 +284,36 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     {
         const __nv_bfloat16 *qb = p.q + (static_cast<int64_t>(b) * p.num_heads + h0) * D;
         const int r0 = lane >> 2;
-        const int c0 = (lane & 3) * 2;
+        if constexpr (FP8) {
+            // f16, head dims permuted as the K fragments deliver them: MMA k 2j, 2j+1 are
+            // dims 4j, 4j+1 and k 2j+8, 2j+9 are dims 4j+2, 4j+3 of the 16-dim step
+            // (j = lane % 4).  |q| is clamped to the f16 range.
+            const int c0 = (lane & 3) * 4;
+            auto f16pair = [](uint32_t w) -> uint32_t {
+                const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
+                const float hi = fminf(fmaxf(__uint_as_float(w & 0xffff0000u), -65504.f), 65504.f);
+                return pack_f16x2(lo, hi);
+            };
 #pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-            qa[ks][0] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0) : 0u;
-            qa[ks][1] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0) : 0u;
-            qa[ks][2] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0 + 8) : 0u;
-            qa[ks][3] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0 + 8) : 0u;
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint2 x0 = make_uint2(0u, 0u), x1 = make_uint2(0u, 0u);
+                if (r0 < rows_valid) x0 = *reinterpret_cast<const uint2 *>(qb + r0 * D + ks * 16 + c0);
+                if (r0 + 8 < rows_valid)
+                    x1 = *reinterpret_cast<const uint2 *>(qb + (r0 + 8) * D + ks * 16 + c0);
+                qa[ks][0] = f16pair(x0.x);
+                qa[ks][1] = f16pair(x1.x);
+                qa[ks][2] = f16pair(x0.y);
+                qa[ks][3] = f16pair(x1.y);
+            }
+        } else {
+            const int c0 = (lane & 3) * 2;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                qa[ks][0] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0) : 0u;
+                qa[ks][1] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0) : 0u;
+                qa[ks][2] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0 + 8) : 0u;
+                qa[ks][3] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0 + 8) : 0u;
+            }
         }
     }
 
@@ -259,7 +321,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     const int u_last = (hi - 1) >> 4;
     const int32_t *bt_row = p.block_table + static_cast<int64_t>(b) * p.max_num_blocks;
     const int bs_mask = (1 << p.log2_bs) - 1;
-    uint8_t *my_stages = smem + warp * NSTAGES * STAGE_BYTES;
+    uint8_t *my_stages = smem + warp * NSTAGES * STAGE_BYTES;  // NST stages of SB bytes
     const uint32_t stage_base = smem_u32(my_stages);
     const uint64_t policy = l2_policy_evict_first();
 
@@ -270,11 +332,17 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
 
     auto issue = [&](int u, int st) {
         if constexpr (FP8) {
-            // fp8 rows, 16-byte chunks, no swizzle (the conversion reads them in order).
+            // fp8 rows of D bytes, 16-byte chunks, swizzled (swz8).
             const uint32_t sb = stage_base + st * STAGE8;
             const int c = lane % CPR8;
             const int rsub = lane / CPR8;
             const int j0 = u * 16;
+            int blk0 = 0;
+            bool blk0_ok = false;
+            if (page_units) {
+                blk0 = __ldg(bt_row + (j0 >> p.log2_bs));
+                blk0_ok = blk0 >= 0 && blk0 < p.num_blocks;
+            }
 #pragma unroll
             for (int i = 0; i < PASSES8; ++i) {
                 const int r = i * RPP8 + rsub;
@@ -282,8 +350,8 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
                 int64_t off = 0;
                 uint32_t nbytes = 0;
                 if (j >= lo && j < hi) {
-                    const int blk = __ldg(bt_row + (j >> p.log2_bs));
-                    if (blk < 0 || blk >= p.num_blocks) {
+                    const int blk = page_units ? blk0 : __ldg(bt_row + (j >> p.log2_bs));
+                    if (page_units ? !blk0_ok : (blk < 0 || blk >= p.num_blocks)) {
                         flag_error(p.err, kErrBlockRange);
                     } else {
                         off = (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
@@ -291,7 +359,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
                         nbytes = 16;
                     }
                 }
-                const uint32_t so = r * D + c * 16;
+                const uint32_t so = r * D + (swz8<D>(c, r) << 4);
                 cp_async_16_policy(sb + so, p.k8 + off, nbytes, policy);
                 cp_async_16_policy(sb + TILE8 + so, p.v8 + off, nbytes, policy);
             }
@@ -352,9 +420,9 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     float l_run[2] = {0.f, 0.f};
 
     const int my_first = u_first + warp;
-    // Prologue: NSTAGES - 1 units in flight.
+    // Prologue: NST - 1 units in flight.
 #pragma unroll
-    for (int st = 0; st < NSTAGES - 1; ++st) {
+    for (int st = 0; st < NST - 1; ++st) {
         const int u = my_first + st * NWARPS;
         if (u <= u_last) issue(u, st);
         cp_async_commit();
@@ -363,56 +431,37 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     int it = 0;
     for (int u = my_first; u <= u_last; u += NWARPS, ++it) {
         {
-            const int un = u + (NSTAGES - 1) * NWARPS;
-            if (un <= u_last) issue(un, (it + NSTAGES - 1) % NSTAGES);
+            const int un = u + (NST - 1) * NWARPS;
+            if (un <= u_last) issue(un, (it + NST - 1) % NST);
             cp_async_commit();
         }
-        cp_async_wait<NSTAGES - 1>();
+        cp_async_wait<NST - 1>();
         __syncwarp();
 
-        uint32_t kb = stage_base + (it % NSTAGES) * STAGE_BYTES;
-        if constexpr (FP8) {
-            // E4M3 -> bf16 into this warp's conversion tile (same swizzled layout as a
-            // bf16 stage): fp8 chunk c of row r becomes bf16 chunks 2c and 2c + 1.
-            const uint32_t src = stage_base + (it % NSTAGES) * STAGE8;
-            kb = stage_base + NSTAGES * STAGE8;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {  // K then V
-#pragma unroll
-                for (int q = lane; q < 16 * CPR8; q += 32) {
-                    const int r = q / CPR8;
-                    const int c = q - r * CPR8;
-                    uint32_t x0, x1, x2, x3;
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                                 : "r"(src + t * TILE8 + r * D + c * 16));
-                    const uint32_t xs[4] = {x0, x1, x2, x3};
-                    uint32_t y[8];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        y[2 * k] = e4m3x2_to_bf16x2(xs[k] & 0xffffu);
-                        y[2 * k + 1] = e4m3x2_to_bf16x2(xs[k] >> 16);
-                    }
-                    const uint32_t dst = kb + t * TILE_BYTES + r * ROWB;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     dst + (((2 * c) ^ (r & 7)) << 4)),
-                                 "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     dst + (((2 * c + 1) ^ (r & 7)) << 4)),
-                                 "r"(y[4]), "r"(y[5]), "r"(y[6]), "r"(y[7])
-                                 : "memory");
-                }
-            }
-            __syncwarp();
-        }
-        const uint32_t vb = kb + TILE_BYTES;
+        const uint32_t kb = stage_base + (it % NST) * SB;
+        const uint32_t vb = kb + (FP8 ? TILE8 : TILE_BYTES);
 
         // S = Q K^T for 16 keys: two n-tiles of 8 keys, even and odd k-steps in
         // separate accumulators to halve the dependent MMA chain.
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
+        if constexpr (FP8) {
+            // One ldmatrix.x4 covers 16 keys x 32 head dims (two k-steps); each 32-bit
+            // word holds 4 consecutive dims of one key: two f16 pairs, b0 and b1.
+            const int r = ((lane >> 4) << 3) + (lane & 7);
+            const int chi = (lane >> 3) & 1;
+#pragma unroll
+            for (int kq = 0; kq < D / 32; ++kq) {
+                uint32_t kw[4];
+                ldmatrix_x4(kw, kb + r * D + (swz8<D>(2 * kq + chi, r) << 4));
+                mma_f16_16816(s[0], qa[2 * kq], e4m3x2_to_f16x2(kw[0]), e4m3x2_to_f16x2(kw[0] >> 16));
+                mma_f16_16816(s[1], qa[2 * kq], e4m3x2_to_f16x2(kw[2]), e4m3x2_to_f16x2(kw[2] >> 16));
+                mma_f16_16816(s2[0], qa[2 * kq + 1], e4m3x2_to_f16x2(kw[1]),
+                              e4m3x2_to_f16x2(kw[1] >> 16));
+                mma_f16_16816(s2[1], qa[2 * kq + 1], e4m3x2_to_f16x2(kw[3]),
+                              e4m3x2_to_f16x2(kw[3] >> 16));
+            }
+        } else {
             const int r = ((lane >> 4) << 3) + (lane & 7);
             const int chi = (lane >> 3) & 1;
 #pragma unroll
@@ -480,20 +529,50 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
             s[nt][2] = ex2_approx(s[nt][2] - m_use1);
             s[nt][3] = ex2_approx(s[nt][3] - m_use1);
         }
-        // P as the A operand straight from the S accumulators; the denominator sums the
-        // bf16 weights the MMA actually uses.
+        // P as the A operand straight from the S accumulators (f16 for the FP8 cache);
+        // the denominator sums the rounded weights the MMA actually uses.
         uint32_t pa[4];
-        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-        l_run[0] += __uint_as_float(pa[0] << 16) + __uint_as_float(pa[0] & 0xffff0000u) +
-                    __uint_as_float(pa[2] << 16) + __uint_as_float(pa[2] & 0xffff0000u);
-        l_run[1] += __uint_as_float(pa[1] << 16) + __uint_as_float(pa[1] & 0xffff0000u) +
-                    __uint_as_float(pa[3] << 16) + __uint_as_float(pa[3] & 0xffff0000u);
+        if constexpr (FP8) {
+            pa[0] = pack_f16x2(s[0][0], s[0][1]);
+            pa[1] = pack_f16x2(s[0][2], s[0][3]);
+            pa[2] = pack_f16x2(s[1][0], s[1][1]);
+            pa[3] = pack_f16x2(s[1][2], s[1][3]);
+            add_f16x2_f32(l_run[0], pa[0]);
+            add_f16x2_f32(l_run[0], pa[2]);
+            add_f16x2_f32(l_run[1], pa[1]);
+            add_f16x2_f32(l_run[1], pa[3]);
+        } else {
+            pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+            pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+            pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+            pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+            l_run[0] += __uint_as_float(pa[0] << 16) + __uint_as_float(pa[0] & 0xffff0000u) +
+                        __uint_as_float(pa[2] << 16) + __uint_as_float(pa[2] & 0xffff0000u);
+            l_run[1] += __uint_as_float(pa[1] << 16) + __uint_as_float(pa[1] & 0xffff0000u) +
+                        __uint_as_float(pa[3] << 16) + __uint_as_float(pa[3] & 0xffff0000u);
+        }
 
         // O += P V.
-        {
+        if constexpr (FP8) {
+            // ldmatrix.trans on byte pairs: a word holds (key 2j, dims 2c', 2c'+1) and
+            // (key 2j+1, same dims); one byte permute makes the key pairs of dim 2c' and
+            // of dim 2c'+1.  o[4 dq + 2 h + e] holds dims 32 dq + 16 h + 2 n + e.
+            const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
+            const int chi = lane >> 4;
+#pragma unroll
+            for (int dq = 0; dq < D / 32; ++dq) {
+                uint32_t vw[4];
+                ldmatrix_x4_trans(vw, vb + r * D + (swz8<D>(2 * dq + chi, r) << 4));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x0 = __byte_perm(vw[2 * h], 0u, 0x3120);      // keys 0-7
+                    const uint32_t x1 = __byte_perm(vw[2 * h + 1], 0u, 0x3120);  // keys 8-15
+                    mma_f16_16816(o[4 * dq + 2 * h], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
+                    mma_f16_16816(o[4 * dq + 2 * h + 1], pa, e4m3x2_to_f16x2(x0 >> 16),
+                                  e4m3x2_to_f16x2(x1 >> 16));
+                }
+            }
+        } else {
             const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
             const int chi = lane >> 4;
 #pragma unroll
@@ -532,12 +611,24 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
             l_s[warp * 16 + r0 + 8] = l_run[1];
         }
         float *ow = o_s + warp * 16 * OSTRIDE;
+        if constexpr (FP8) {
 #pragma unroll
-        for (int dt = 0; dt < DTILES; ++dt) {
-            const int d = dt * 8 + (lane & 3) * 2;
-            *reinterpret_cast<float2 *>(ow + r0 * OSTRIDE + d) = make_float2(o[dt][0], o[dt][1]);
-            *reinterpret_cast<float2 *>(ow + (r0 + 8) * OSTRIDE + d) =
-                make_float2(o[dt][2], o[dt][3]);
+            for (int dt = 0; dt < DTILES; ++dt) {
+                // dt = 4 dq + 2 h + e: dims 32 dq + 16 h + 4 (lane % 4) + e and + 2
+                const int d = (dt >> 2) * 32 + ((dt >> 1) & 1) * 16 + (lane & 3) * 4 + (dt & 1);
+                ow[r0 * OSTRIDE + d] = o[dt][0];
+                ow[r0 * OSTRIDE + d + 2] = o[dt][1];
+                ow[(r0 + 8) * OSTRIDE + d] = o[dt][2];
+                ow[(r0 + 8) * OSTRIDE + d + 2] = o[dt][3];
+            }
+        } else {
+#pragma unroll
+            for (int dt = 0; dt < DTILES; ++dt) {
+                const int d = dt * 8 + (lane & 3) * 2;
+                *reinterpret_cast<float2 *>(ow + r0 * OSTRIDE + d) = make_float2(o[dt][0], o[dt][1]);
+                *reinterpret_cast<float2 *>(ow + (r0 + 8) * OSTRIDE + d) =
+                    make_float2(o[dt][2], o[dt][3]);
+            }
         }
     }
     __syncthreads();
