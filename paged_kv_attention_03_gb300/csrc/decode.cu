@@ -22,7 +22,11 @@
 //  * Online softmax in the base-2 domain with 2-step warp shuffles per row; the
 //    warps of a CTA merge their (m, l, O) through shared memory; a split writes
 //    either the final bf16 row (single split) or a normalised fp32 partial plus
-//    (m, l) to the workspace for decode_combine_kernel.
+//    (m, l) to the workspace for decode_combine_kernel, which is launched with
+//    programmatic stream serialization so its launch overlaps the splits' tail.
+//  * Three CTAs per SM (2-stage rings, <= 168 registers) hide each other's pipeline
+//    fill; the FP8 instantiation keeps the codes fp8 in shared memory and runs f16
+//    MMAs on codes converted in registers.
 #include <math.h>
 
 #include <cuda_fp16.h>
