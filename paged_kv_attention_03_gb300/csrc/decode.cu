@@ -814,6 +814,11 @@ bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int m
         int64_t s = (target + units - 1) / units;
         const int64_t by_len = (span + 255) / 256;
         if (s > by_len) s = by_len;
+        // Long contexts: 8192-key chunks amortise each CTA's fixed cost (fill, merge)
+        // better, as long as they still give two waves of resident CTAs.
+        const int64_t s_long = (span + 8191) / 8192;
+        if (s_long >= 2 && s_long < s && units * s_long >= 2LL * kDecodeCtasPerSm * 152)
+            s = s_long;
         splits = static_cast<int>(s);
     }
     if (splits < 1) splits = 1;
