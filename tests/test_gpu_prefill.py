@@ -91,6 +91,32 @@ def test_prefill_tile_edges(cuda, lens):
                                        seed=46, device=cuda), cuda)
 
 
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (32, 8)])
+def test_prefill_many_sequences(cuda, H, Hkv):
+    # 150 sequences of 1..300 query tokens (some with a cached context): the work list
+    # has far more (query block, sequence) pairs than one 32-pair scan window, most of
+    # the longest-first positions are empty, and every row is checked.
+    w = Workload("many", H, Hkv, 128, 16, ())
+    rng = np.random.default_rng(7)
+    q = rng.integers(1, 301, size=150)
+    ctx = np.where(rng.random(150) < 0.3, rng.integers(0, 200, size=150), 0)
+    _full_check(make_case_from_lengths(w, ctx, q, seed=52, device=cuda), cuda)
+
+
+def test_prefill_late_bad_sequence_is_flagged(cuda):
+    # A sequence far down the work list with more queries than keys is reported too.
+    w = Workload("late", 8, 2, 128, 16, ())
+    case = make_case_from_lengths(w, [0] * 200, [40] * 200, seed=53, device=cuda)
+    m = device_tensors(case, cuda)
+    bad = case.seq_lens.copy()
+    bad[187] = 10  # 40 queries, 10 keys
+    pa.pa_read_device_error(clear=True, device=cuda)
+    pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"],
+                         torch.as_tensor(bad, device=cuda), m["block_table"], 40, 40,
+                         w.final_scale, 0)
+    assert pa.pa_read_device_error(clear=True, device=cuda) & pa.DEVERR_QUERY_LEN
+
+
 def test_prefill_cu_seqlens_k_instead_of_seq_lens(cuda):
     case = make_case("mixed_window_small", seed=47, device=cuda)
     _full_check(case, cuda, use_cu_k=True)
