@@ -151,7 +151,8 @@ struct Layout {
 // Geometry of one work item; every role derives it identically.
 struct Item {
     bool valid;
-    bool has1;  // the second query tile has rows
+    bool has1;       // the second query tile has rows
+    bool half_last;  // no row sees the upper 64 keys of the last K/V tile
     int seq, kvh, q0, rows0, rows1, q_start, sq, sk, kt0, n_tiles;
     int split;  // shared-prefix mode: key split of the item
 };
@@ -181,6 +182,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
         it.sk = p.prefix_len;
         it.valid = false;
         it.has1 = false;
+        it.half_last = false;
         const int T = p.tok_per_tile;
         it.q0 = qi * 2 * T;
         if (it.q0 >= it.sq) return it;
@@ -191,6 +193,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
         it.kt0 = it.split * p.chunk_tiles;
         it.n_tiles = min(p.chunk_tiles, total_tiles - it.kt0);
         it.valid = it.n_tiles > 0;
+        it.half_last = p.prefix_len - 1 < (it.kt0 + it.n_tiles - 1) * BN + BN / 2;
         return it;
     }
     const int per_q = p.num_kv_heads * p.num_seqs;
@@ -200,6 +203,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
     it.kvh = rem - it.seq * p.num_kv_heads;
     it.valid = false;
     it.has1 = false;
+    it.half_last = false;
     it.q_start = p.cu_q[it.seq];
     it.sq = p.cu_q[it.seq + 1] - it.q_start;
     int sk;
@@ -230,6 +234,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
     const int kmin = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
     it.kt0 = kmin / BN;
     it.n_tiles = p_hi / BN - it.kt0 + 1;
+    it.half_last = p_hi < (it.kt0 + it.n_tiles - 1) * BN + BN / 2;
     it.valid = true;
     return it;
 }
@@ -562,6 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Order on the tensor pipe, across items: P0 V(g-1), S0(g), P1 V(g-1), S1(g).
             if (lane == 0) {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+                // Half tile: the item's last K/V tile when no row sees its upper 64 keys
+                // (diagonal of a query block that ends in the tile's lower half): S over
+                // 64 keys, P V over 64 keys.  The softmax needs no change: the causal mask
+                // already sets columns 64..127 to -inf.
+                constexpr uint32_t idesc_s_half = idesc_bf16_f32(BM, BN / 2, false);
                 constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
                 uint32_t g = 0;                  // global KV tile counter
                 uint32_t cnt[2] = {0, 0};        // tiles issued per query tile (S / P V)
@@ -569,9 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 // Pending P V of the previous KV tile: its V stage, whether it is the first tile
                 // of its item (overwrite O), and whether query tile 1 takes part.
-                bool have_prev = false, prev_first = false, prev_has1 = false;
+                bool have_prev = false, prev_first = false, prev_has1 = false, prev_half = false;
                 uint32_t prev_g = 0;
-                auto issue_pv = [&](int i, uint32_t gv, bool first) -> bool {
+                auto issue_pv = [&](int i, uint32_t gv, bool first, bool half) -> bool {
                     const uint32_t c = cnt[i]++;
                     if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err)) return false;
                     if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err))
@@ -580,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vbase = sV + (gv % NSV) * L::TILE;
     #pragma unroll
                     for (int k = 0; k < KSTEPS_O; ++k) {
+                        if (half && k >= KSTEPS_O / 2) break;
                         const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
                         mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, b, idesc_o,
                                     (!first || k > 0) ? 1u : 0u);
@@ -587,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar(B_ODONE + i));
                     return true;
                 };
-                auto issue_s = [&](int i, uint32_t gk) {
+                auto issue_s = [&](int i, uint32_t gk, bool half) {
                     const uint32_t qbase = sQ + i * L::TILE;
                     const uint32_t kbase = sK + (gk % NSK) * L::TILE;
     #pragma unroll
@@ -595,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
                         const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
                         const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                        mma_bf16_ss(tmem + col_s(i), a, b, idesc_s, k > 0);
+                        mma_bf16_ss(tmem + col_s(i), a, b, half ? idesc_s_half : idesc_s, k > 0);
                     }
                     mma_commit(bar(B_SFULL + i));
                 };
@@ -603,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto flush = [&]() -> bool {
                     if (!have_prev) return true;
                     have_prev = false;
-                    if (!issue_pv(0, prev_g, prev_first)) return false;
-                    if (prev_has1 && !issue_pv(1, prev_g, prev_first)) return false;
+                    if (!issue_pv(0, prev_g, prev_first, prev_half)) return false;
+                    if (prev_has1 && !issue_pv(1, prev_g, prev_first, prev_half)) return false;
                     mma_commit(bar(B_VEMPTY + prev_g % NSV));
                     return true;
                 };
@@ -627,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st = g % NSK;
                         // query tile 0: P0 V of the previous tile needs no K, so it goes to
                         // the tensor core before the wait for K(g)
-                        if (have_prev && !issue_pv(0, prev_g, prev_first)) {
+                        const bool half = it.half_last && j == it.n_tiles - 1;
+                        if (have_prev && !issue_pv(0, prev_g, prev_first, prev_half)) {
                             ok = false;
                             break;
                         }
@@ -636,20 +648,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        issue_s(0, g);
+                        issue_s(0, g, half);
                         // query tile 1
-                        if (have_prev && prev_has1 && !issue_pv(1, prev_g, prev_first)) {
+                        if (have_prev && prev_has1 && !issue_pv(1, prev_g, prev_first, prev_half)) {
                             ok = false;
                             break;
                         }
                         if (have_prev) mma_commit(bar(B_VEMPTY + prev_g % NSV));
-                        if (it.has1) issue_s(1, g);
+                        if (it.has1) issue_s(1, g, half);
                         mma_commit(bar(B_KEMPTY + st));
                         if (j == it.n_tiles - 1) mma_commit(bar(B_QEMPTY));
                         have_prev = true;
                         prev_g = g;
                         prev_first = j == 0;
                         prev_has1 = it.has1;
+                        prev_half = half;
                     }
                     if (!ok) break;
                 }
