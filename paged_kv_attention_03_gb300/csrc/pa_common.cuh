@@ -24,12 +24,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte async global->shared copy; src_bytes == 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
 
 __device__ __forceinline__ void cp_async_16_policy(uint32_t dst, const void *src,
                                                    uint32_t src_bytes, uint64_t policy) {

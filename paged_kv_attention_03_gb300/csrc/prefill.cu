@@ -71,8 +71,6 @@ constexpr uint32_t kRing = 8;   // item-info ring slots
 constexpr uint32_t kAhead = 6;  // items published beyond the last Q load
 constexpr int kThreads = 12 * 32;
 constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 96;
-// Bit (i % 8) set: column pair i of a logit row takes 2^x from the cubic on the FMA pipe.
-constexpr uint32_t kPolyPairs = 0x00u;
 static_assert(kRegsSoftmax * 256 + kRegsProducer * 128 <= 168 * kThreads,
               "register split exceeds the launch's 168 per thread");
 constexpr uint32_t kTmemCols = 512;
@@ -782,9 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // P = 2^(s * scale_log2 - m) as bf16 over the low 64 columns of S; the
                 // denominator sums the bf16 weights the MMA actually uses.
-                // Pairs of columns go through packed f32x2 arithmetic; the pairs picked by
-                // kPolyPairs take 2^x on the FMA pipe, the rest on the MUFU unit, which
-                // would otherwise bound the tile.
+                // Pairs of columns go through packed f32x2 arithmetic; 2^x on the MUFU unit
+                // (moving part of it to a polynomial on the FMA pipe measured slower: the
+                // softmax is bound by instruction issue).
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_use, -m_use);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums of the bf16 weights
@@ -795,16 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) {
                         const uint64_t x = f2_fma(f2_pack(s[cc * 64 + 2 * i], s[cc * 64 + 2 * i + 1]),
                                                   sl2x2, negm2);
-                        float e0, e1;
-                        if ((kPolyPairs >> (i & 7)) & 1u) {
-                            exp2_fma_x2(x, e0, e1);
-                        } else {
-                            float x0, x1;
-                            f2_unpack(x, x0, x1);
-                            e0 = ex2_approx(x0);
-                            e1 = ex2_approx(x1);
-                        }
-                        pk[i] = pack_bf16x2(e0, e1);
+                        float x0, x1;
+                        f2_unpack(x, x0, x1);
+                        pk[i] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
                         add_bf16x2_f32(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], pk[i]);
                     }
                     tmem_st_32x32b_x32_u(scol + cc * 32, pk);

@@ -154,9 +154,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -274,15 +271,6 @@ __device__ __forceinline__ void tmem_wait_ld_regs(float (&v)[32]) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_32x32b_x16_u(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15])
-        : "memory");
-}
 
 }  // namespace sm100
 }  // namespace pa
@@ -290,50 +278,11 @@ __device__ __forceinline__ void tmem_st_32x32b_x16_u(uint32_t taddr, const uint3
 namespace pa {
 namespace sm100 {
 
-// ---------------------------------------------------------------- clusters ---
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
 
-__device__ __forceinline__ uint32_t num_clusters_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
 
-// All threads of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
-}
 
-// TMA tile load delivered to the same shared-memory offset in every CTA of `mask`, each
-// destination's mbarrier (same offset) receiving the complete_tx of its copy.
-__device__ __forceinline__ void tma_load_3d_mcast(uint32_t dst, const void *tmap, int c0, int c1,
-                                                  int c2, uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(mask)
-        : "memory");
-}
 
-// Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when all tcgen05
-// operations this thread issued so far are done.
-__device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
 
 }  // namespace sm100
 }  // namespace pa
@@ -377,11 +326,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 // lo += float(bf16 low half of v), hi += float(bf16 high half of v): the mixed-precision
 // add takes the bf16 halves directly (bf16 -> f32 is exact, the add rounds to nearest).
 __device__ __forceinline__ void add_bf16x2_f32(float &lo, float &hi, uint32_t v) {
@@ -400,30 +344,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-// 2^x for a pair of x <= 127 on the FMA pipe instead of the MUFU unit (the exponential
-// unit is the softmax's bottleneck, so part of the work moves here).  x is clamped at
-// -126, split as x = j + f with j = round(x) (adding 1.5 * 2^23 leaves round(x) in the
-// low mantissa bits) and f in [-0.5, 0.5]; 2^f comes from a cubic fitted to it on that
-// interval (iteratively reweighted least squares on the relative error, max relative
-// error 7.5e-5, far below the bf16 rounding of P); 2^j is added to the exponent field.
-__device__ __forceinline__ void exp2_fma_x2(uint64_t x2, float &r0, float &r1) {
-    float x0, x1;
-    f2_unpack(x2, x0, x1);
-    const uint64_t xc = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-    const uint64_t magic = f2_pack(12582912.f, 12582912.f);
-    const uint64_t y = f2_add(xc, magic);
-    const uint64_t j = f2_add(y, f2_pack(-12582912.f, -12582912.f));
-    const uint64_t f = f2_fma(j, f2_pack(-1.f, -1.f), xc);
-    uint64_t poly = f2_fma(f, f2_pack(0.05517195910215378f, 0.05517195910215378f),
-                           f2_pack(0.2426111400127411f, 0.2426111400127411f));
-    poly = f2_fma(poly, f, f2_pack(0.693260908126831f, 0.693260908126831f));
-    poly = f2_fma(poly, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
-    float p0, p1, y0, y1;
-    f2_unpack(poly, p0, p1);
-    f2_unpack(y, y0, y1);
-    r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(y0) << 23));
-    r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(y1) << 23));
-}
 
 }  // namespace sm100
 }  // namespace pa
