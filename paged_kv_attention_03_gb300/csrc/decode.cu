@@ -201,6 +201,14 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Speculative block-table entry of this warp's first 16-key unit for a range that
+    // starts at key 0 (no window, no key_begin): loaded together with seq_lens, so the
+    // first K/V copies need one memory round trip less.  Used only if it is that unit.
+    const int spec_unit = ((split * p.chunk) >> 4) + static_cast<int>(threadIdx.x >> 5);
+    int spec_blk = 0;
+    if (p.log2_bs >= 4 && ((spec_unit << 4) >> p.log2_bs) < p.max_num_blocks)
+        spec_blk = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_num_blocks +
+                         ((spec_unit << 4) >> p.log2_bs));
     const bool report = split == 0 && blockIdx.y == 0 && threadIdx.x == 0;
     const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
                                      p.key_begin ? p.key_begin[b] : p.key_begin_all, p.err,
@@ -334,6 +342,10 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     const bool page_units = p.log2_bs >= 4;
     const int64_t row_stride = static_cast<int64_t>(p.num_kv_heads) * D;
 
+    // The block of 16-key unit u (block_size >= 16: one lookup per unit).
+    auto unit_block = [&](int u) -> int {
+        return u == spec_unit ? spec_blk : __ldg(bt_row + ((u << 4) >> p.log2_bs));
+    };
     auto issue = [&](int u, int st) {
         if constexpr (FP8) {
             // fp8 rows of D bytes, 16-byte chunks, swizzled (swz8).
@@ -344,7 +356,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
             int blk0 = 0;
             bool blk0_ok = false;
             if (page_units) {
-                blk0 = __ldg(bt_row + (j0 >> p.log2_bs));
+                blk0 = unit_block(u);
                 blk0_ok = blk0 >= 0 && blk0 < p.num_blocks;
             }
 #pragma unroll
@@ -375,7 +387,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
         const int j0 = u * 16;
         if (page_units) {
             const bool full = j0 >= lo && j0 + 16 <= hi;
-            const int blk = __ldg(bt_row + (j0 >> p.log2_bs));
+            const int blk = unit_block(u);
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             if (!blk_ok && lane == 0) flag_error(p.err, kErrBlockRange);
             const int64_t base =
