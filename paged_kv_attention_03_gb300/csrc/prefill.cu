@@ -30,11 +30,12 @@
 //    so each softmax warpgroup works on its tile while the tensor core runs the other
 //    tile's products (ping-pong).
 //  * Warp roles: 0-3 and 4-7 are the two softmax warpgroups (200 registers each after
-//    setmaxnreg), 8 loads K, 9 issues MMAs, 10 loads V, 11 schedules the CTA's items and
-//    loads Q (96 registers); the softmax
-//    warpgroups (thread = TMEM lane = accumulator row): mask, online softmax in
-//    base 2 with the scale folded into the exponent, lazy O rescale (only when the
-//    running max grows by more than 2^8), epilogue.
+//    setmaxnreg); 8 loads K, 9 issues MMAs, 10 loads V, 11 schedules the CTA's items and
+//    loads Q (96 registers).  A softmax thread owns one TMEM lane (accumulator row):
+//    mask, online softmax in base 2 with the scale folded into the exponent, lazy O
+//    rescale (only when the running max grows by more than 2^8), epilogue.
+//  * The K and V producers issue one page box per lane, in parallel; an item's last K/V
+//    tile runs at half width (64 keys) when no row of the item sees its upper half.
 //  * Every mbarrier wait is bounded: on timeout the CTA raises an error bit, drains,
 //    frees its tensor memory and returns.
 #include <cuda.h>
