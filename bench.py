@@ -666,7 +666,7 @@ def _cascade_leg(pa, dev, rank, peaks, flush, stream, args):
     return {"workload": "shared_prefix: 64 requests, prefix 4096 + own suffix U[128,1024], "
                         "32/8 heads, D=128, bs=16",
             "logical_bytes": r.logical_bytes, "physical_bytes": r.physical_bytes,
-            "cascade": {"ms_per_step": round(tc, 4), "launches": 4,
+            "cascade": {"ms_per_step": round(tc, 4), "launches": 3,
                         "effective_gbs": round(r.logical_bytes / (tc / 1e3) / 1e9, 1),
                         "physical_gbs": round(r.physical_bytes / (tc / 1e3) / 1e9, 1),
                         "physical_frac_of_hbm": round(r.physical_bytes / (tc / 1e3) / 1e9 /

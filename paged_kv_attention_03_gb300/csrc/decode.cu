@@ -86,6 +86,10 @@ struct DecodeKernelParams {
     float kv_scale;
     float *st_o;
     float *st_lse;
+    // Extra partial states the combine merges in (pre_parts x [batch * num_heads] rows).
+    const float *pre_o;
+    const float *pre_lse;
+    int pre_parts;
     unsigned *err;
 };
 
@@ -697,7 +701,9 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     const int nsplit = sr.L > sr.start ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
     const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h;
     __nv_bfloat16 *dst = p.out + bh * D + lane * PER_LANE;
-    if (nsplit == 0) {
+    const int npre = p.pre_parts;
+    const int64_t pre_rows = static_cast<int64_t>(batch) * p.num_heads;
+    if (nsplit == 0 && npre == 0) {
         if (p.st_o != nullptr) {
 #pragma unroll
             for (int i = 0; i < PER_LANE; ++i) p.st_o[bh * D + lane * PER_LANE + i] = 0.f;
@@ -717,7 +723,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
         const float m = s < nsplit ? ml[2 * s] : -INFINITY;
         M = fmaxf(M, m);
     }
+    // Extra parts: log2 of their softmax mass is lse / ln 2.
+    for (int r0 = 0; r0 < npre; r0 += 32) {
+        const int r = r0 + lane;
+        M = fmaxf(M, r < npre ? p.pre_lse[r * pre_rows + bh] * kLog2e : -INFINITY);
+    }
     M = warp_max(M);
+    if (M == -INFINITY) M = 0.f;  // every part empty: all weights are 0
     float wsum = 0.f;
     float acc[PER_LANE];
 #pragma unroll
@@ -744,14 +756,27 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
             }
         }
     }
+    for (int r0 = 0; r0 < npre; r0 += 32) {
+        const int r = r0 + lane;
+        const float wl = r < npre ? ex2_approx(p.pre_lse[r * pre_rows + bh] * kLog2e - M) : 0.f;
+        wsum += wl;
+        const int n = min(32, npre - r0);
+        for (int k = 0; k < n; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            const float *src = p.pre_o + (static_cast<int64_t>(r0 + k) * pre_rows + bh) * D +
+                               lane * PER_LANE;
+#pragma unroll
+            for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
+        }
+    }
     wsum = warp_sum(wsum);
-    const float inv = 1.f / wsum;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     if (p.st_o != nullptr) {
         // Partial state: normalised row and ln(sum_j e^{s_j}) = (M + log2 wsum) ln 2.
         float *so = p.st_o + bh * D + lane * PER_LANE;
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) so[i] = acc[i] * inv;
-        if (lane == 0) p.st_lse[bh] = (M + log2f(wsum)) * kLn2;
+        if (lane == 0) p.st_lse[bh] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
         return;
     }
 #pragma unroll
@@ -780,7 +805,8 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
     e = cudaGetLastError();
-    if (e != cudaSuccess || (plan.num_splits == 1 && kp.st_o == nullptr)) return e;
+    if (e != cudaSuccess || (plan.num_splits == 1 && kp.st_o == nullptr && kp.pre_parts == 0))
+        return e;
     // Programmatic stream serialization: the combine grid launches while the last split
     // CTAs finish, and waits for them on the device.
     const int warps = batch * kp.num_heads;
@@ -876,7 +902,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.scale_log2 = a.scale * kLog2e;
     kp.chunk = plan.chunk;
     kp.num_splits = plan.num_splits;
-    if (plan.num_splits > 1 || a.state_o != nullptr) {
+    if (plan.num_splits > 1 || a.state_o != nullptr || a.pre_parts > 0) {
         const size_t rows = static_cast<size_t>(a.batch) * a.num_heads * plan.num_splits;
         const size_t o_bytes = (rows * a.head_dim * sizeof(float) + 255) / 256 * 256;
         kp.ws_o = static_cast<float *>(a.workspace);
@@ -894,6 +920,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.key_begin_all = a.key_begin_all;
     kp.st_o = a.state_o;
     kp.st_lse = a.state_lse;
+    kp.pre_o = a.pre_o;
+    kp.pre_lse = a.pre_lse;
+    kp.pre_parts = a.pre_parts;
     kp.err = a.err;
     if (a.fp8) {
         // E4M3 caches: codes read through the byte views, kv_scale on the scores (K) and,

@@ -295,8 +295,8 @@ static bool suffix_plan(int batch, int num_heads, int num_kv_heads, int head_dim
                            plan);
 }
 
-// Cascade workspace: R = prefix splits + 1 parts of [rows, head_dim] fp32 and [rows] lse,
-// then the suffix decode's own split-K workspace.
+// Cascade workspace: the prefix splits' parts ([rows, head_dim] fp32 and [rows] lse each),
+// then the suffix decode's own split-K workspace (its combine merges the prefix parts).
 struct CascadeLayout {
     int n_splits = 0, chunk_tiles = 1;
     size_t states = 0, lses = 0, decode_ws = 0, decode_need = 0, total = 0;
@@ -312,7 +312,7 @@ static bool cascade_layout(int batch, int num_heads, int num_kv_heads, int head_
                      sliding_window, &plan))
         return false;
     const size_t rows = static_cast<size_t>(batch) * num_heads;
-    const size_t parts = static_cast<size_t>(c->n_splits) + 1;
+    const size_t parts = static_cast<size_t>(c->n_splits) > 0 ? c->n_splits : 1;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     c->states = 0;
     c->lses = up(parts * rows * head_dim * sizeof(float));
@@ -370,7 +370,6 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *states = reinterpret_cast<float *>(ws + c.states);
     float *lses = reinterpret_cast<float *>(ws + c.lses);
-    const int64_t rows = static_cast<int64_t>(batch) * num_heads;
     unsigned *err = device_error_word();
     // 1. The prefix, attended once for every request: parts 0 .. n_splits - 1.
     if (c.n_splits > 0) {
@@ -420,20 +419,13 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const
     a.scale = scale;
     a.workspace = ws + c.decode_ws;
     a.key_begin_all = prefix_len;
-    a.state_o = states + static_cast<int64_t>(c.n_splits) * rows * head_dim;
-    a.state_lse = lses + static_cast<int64_t>(c.n_splits) * rows;
+    // The suffix's split combine also merges the prefix parts and writes the bf16 rows.
+    a.out = out;
+    a.pre_o = states;
+    a.pre_lse = lses;
+    a.pre_parts = c.n_splits;
     a.err = err;
-    pa_status st = from_cuda(pa::launch_decode(a, plan, s));
-    if (st != PA_OK) return st;
-    // 3. Merge the parts.
-    pa::MergeArgs m{};
-    m.out = out;
-    m.states = states;
-    m.lses = lses;
-    m.num_states = c.n_splits + 1;
-    m.rows = rows;
-    m.head_dim = head_dim;
-    return from_cuda(pa::launch_merge_states(m, s));
+    return from_cuda(pa::launch_decode(a, plan, s));
 }
 
 int pa_common_prefix_blocks(const int32_t *block_table, int batch, int max_num_blocks,

@@ -73,6 +73,12 @@ struct DecodeArgs {
     float kv_scale;
     float *state_o;                // [batch, num_heads, head_dim]
     float *state_lse;              // [batch, num_heads]
+    // Extra partial states merged into the output by the combine (the cascade's prefix
+    // parts): pre_parts x [batch * num_heads] rows, normalised fp32 rows pre_o and
+    // natural-log denominators pre_lse (-inf: empty).  0 parts: none.
+    const float *pre_o;
+    const float *pre_lse;
+    int pre_parts;
     unsigned *err;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
