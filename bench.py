@@ -260,7 +260,7 @@ class PrefillRunner:
         self.bt = t(case.block_table)
         self.slots = t(case.slot_mapping)
         self.out = torch.empty_like(case.q)
-        self.launches = 2  # the store of the prompt tokens, then the prefill
+        self.launches = 3  # the store of the prompt tokens, the prefill, the single-row decode
         self.work = prefill_flops(case)
 
     def step(self):
@@ -690,7 +690,7 @@ def _mixed_leg(pa, dev, rank, peaks, flush, stream, args):
                         f"{runner.n_decodes} decodes, ctx U[1024,8192], window 4096",
             "chunk_flops": runner.chunk_flops, "decode_bytes": runner.decode_bytes,
             "roofline_ms": round(roof_ms, 4),
-            "single_call": {"ms_per_step": round(single, 4), "launches": 2,
+            "single_call": {"ms_per_step": round(single, 4), "launches": 3,
                             "frac_of_roofline": round(roof_ms / single, 4)},
             "two_calls": {"ms_per_step": round(split, 4), "launches": 2 + runner.dec.launches,
                           "frac_of_roofline": round(roof_ms / split, 4)}}

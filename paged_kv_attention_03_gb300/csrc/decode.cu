@@ -90,6 +90,10 @@ struct DecodeKernelParams {
     const float *pre_o;
     const float *pre_lse;
     int pre_parts;
+    // Varlen layout: sequence b is a decode row only if q_rows[b + 1] - q_rows[b] == 1;
+    // its q / out row is q_rows[b] (null: row b).
+    const int32_t *q_rows;
+    int after_prefill;  // launched as the prefill kernel's programmatic dependent
     unsigned *err;
 };
 
@@ -177,7 +181,7 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // ldmatrix on byte pairs plus one byte permute (even and odd head dims in separate
 // MMAs).  kv_scale is applied to the scores (K) and the results (V); Q and P are f16.
 template <int D, int NWARPS, int NSTAGES, bool FP8>
-__global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
+__device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
@@ -200,6 +204,12 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
 
     const int split = blockIdx.x;
     const int b = blockIdx.z;
+    int qrow = b;  // q / out row of sequence b
+    if (p.q_rows != nullptr) {
+        const int r0 = p.q_rows[b];
+        if (p.q_rows[b + 1] - r0 != 1) return;  // not a single-row sequence
+        qrow = r0;
+    }
     const int kvh = blockIdx.y / p.head_tiles;
     const int ht = blockIdx.y - kvh * p.head_tiles;
     const int warp = threadIdx.x >> 5;
@@ -289,7 +299,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
         // splits the combine kernel writes it.
         if (p.ws_o == nullptr && sr.L == 0) {
             for (int i = threadIdx.x; i < rows_valid * D; i += NWARPS * 32)
-                p.out[(static_cast<int64_t>(b) * p.num_heads + h0) * D + i] =
+                p.out[(static_cast<int64_t>(qrow) * p.num_heads + h0) * D + i] =
                     __float2bfloat16_rn(0.f);
         }
         return;
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
     // Q fragments (A operand, 16 rows = query heads of this tile, zero padded).
     uint32_t qa[KSTEPS][4];
     {
-        const __nv_bfloat16 *qb = p.q + (static_cast<int64_t>(b) * p.num_heads + h0) * D;
+        const __nv_bfloat16 *qb = p.q + (static_cast<int64_t>(qrow) * p.num_heads + h0) * D;
         const int r0 = lane >> 2;
         if constexpr (FP8) {
             // f16, head dims permuted as the K fragments deliver them: MMA k 2j, 2j+1 are
@@ -671,7 +681,8 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
         if constexpr (FP8) res *= p.kv_scale;  // V elements read code * kv_scale
         const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h0 + row;
         if (p.ws_o == nullptr) {
-            p.out[bh * D + d] = __float2bfloat16_rn(res);
+            p.out[(static_cast<int64_t>(qrow) * p.num_heads + h0 + row) * D + d] =
+                __float2bfloat16_rn(res);
         } else {
             p.ws_o[(bh * p.num_splits + split) * D + d] = res;
             if (d == 0) {
@@ -680,6 +691,15 @@ __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_ke
             }
         }
     }
+}
+
+template <int D, int NWARPS, int NSTAGES, bool FP8>
+__global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
+    decode_split_body<D, NWARPS, NSTAGES, FP8>(p);
+    // The single-row (varlen) mode runs as a programmatic dependent of the prefill kernel
+    // of the same call: no CTA finishes before the prefill grid, so work queued later on
+    // the stream stays ordered after both.
+    if (p.after_prefill) sm100::griddep_wait();
 }
 
 // Log-sum-exp merge of the splits of one (sequence, head) per warp:
@@ -803,7 +823,25 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
-    kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
+    if (kp.after_prefill) {
+        // After the prefill kernel, as its programmatic dependent: the CTAs take SMs as
+        // the prefill's persistent CTAs finish (the rows are disjoint; the cache writes
+        // they read were done by the store launch before the prefill).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kDecodeWarps * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, kp);
+        if (e != cudaSuccess) return e;
+    } else {
+        kern<<<grid, kDecodeWarps * 32, smem, stream>>>(kp);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess || (plan.num_splits == 1 && kp.st_o == nullptr && kp.pre_parts == 0))
         return e;
@@ -923,6 +961,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.pre_o = a.pre_o;
     kp.pre_lse = a.pre_lse;
     kp.pre_parts = a.pre_parts;
+    kp.q_rows = a.q_rows;
+    kp.after_prefill = a.after_prefill ? 1 : 0;
     kp.err = a.err;
     if (a.fp8) {
         // E4M3 caches: codes read through the byte views, kv_scale on the scores (K) and,

@@ -79,6 +79,13 @@ struct DecodeArgs {
     const float *pre_o;
     const float *pre_lse;
     int pre_parts;
+    // Varlen layout (null: q / out rows are the sequences): sequence b is processed only
+    // if q_rows[b + 1] - q_rows[b] == 1, with q / out row q_rows[b].
+    const int32_t *q_rows;
+    // Launch the split kernel as a programmatic dependent of the kernel before it (set
+    // only right after the prefill kernel of the same call, which triggers its dependents
+    // once all its CTAs are resident; every split CTA then waits for that grid at exit).
+    bool after_prefill;
     unsigned *err;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);

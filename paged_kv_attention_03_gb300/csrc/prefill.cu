@@ -113,6 +113,8 @@ struct PrefillKernelParams {
     int num_req;
     int prefix_len;
     int chunk_tiles;
+    // Sequences with one query row are left to the decode kernel of the same call.
+    int skip_decode_rows;
     unsigned *err;
 };
 
@@ -222,6 +224,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
         if (report) flag_error(p.err, kErrQueryLen);
         if (it.sq < 0 || it.sq > sk) return it;
     }
+    if (p.skip_decode_rows && it.sq == 1) return it;  // the decode launch's row
     const int T = p.tok_per_tile;
     it.q0 = qi * 2 * T;
     if (it.q0 >= it.sq) return it;
@@ -357,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Every CTA is resident: a programmatic dependent launched after this kernel (the
+    // single-row decode of the same call) may start taking SMs as CTAs finish.
+    griddep_launch_dependents();
     const int bs_mask = (1 << p.log2_bs) - 1;
 
     // Cache row (slot) of the 16-key piece of `it` starting at key k0, or an
@@ -1062,11 +1068,46 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.window = a.sliding_window;
     kp.scale_log2 = a.scale * kLog2e;
     kp.err = a.err;
-    switch (a.head_dim) {
-        case 64: return launch_prefill_d<64, false>(kp, a, stream);
-        case 128: return launch_prefill_d<128, false>(kp, a, stream);
-        default: return cudaErrorInvalidValue;
+    // Sequences with a single query row (decode rows of a mixed batch) would fill one
+    // token of a 128-row tile: with seq_lens given, a single-split decode launch takes
+    // them (it needs no workspace) and the prefill kernel skips them.
+    const bool route = a.seq_lens != nullptr;
+    kp.skip_decode_rows = route ? 1 : 0;
+    const bool prefill_launched = !route || a.max_seqlen_q > 1;
+    if (prefill_launched) {
+        cudaError_t e;
+        switch (a.head_dim) {
+            case 64: e = launch_prefill_d<64, false>(kp, a, stream); break;
+            case 128: e = launch_prefill_d<128, false>(kp, a, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess || !route) return e;
     }
+    DecodePlan plan;
+    if (!plan_decode(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim, a.max_seqlen_k,
+                     a.sliding_window, 1, &plan))
+        return cudaErrorInvalidValue;
+    DecodeArgs d{};
+    d.out = a.out;
+    d.q = a.q;
+    d.k_cache = a.k_cache;
+    d.v_cache = a.v_cache;
+    d.block_table = a.block_table;
+    d.max_num_blocks = a.max_num_blocks;
+    d.seq_lens = a.seq_lens;
+    d.batch = a.num_seqs;
+    d.max_seq_len = a.max_seqlen_k;
+    d.num_blocks = a.num_blocks;
+    d.block_size = a.block_size;
+    d.num_heads = a.num_heads;
+    d.num_kv_heads = a.num_kv_heads;
+    d.head_dim = a.head_dim;
+    d.sliding_window = a.sliding_window;
+    d.scale = a.scale;
+    d.q_rows = a.cu_seqlens_q;
+    d.after_prefill = prefill_launched;
+    d.err = a.err;
+    return launch_decode(d, plan, stream);
 }
 
 void plan_prefix_splits(int num_req, int num_heads, int num_kv_heads, int prefix_len,
