@@ -319,7 +319,9 @@ int pa_common_prefix_blocks(const int32_t *block_table, int batch, int max_num_b
  * cu_seqlens_k[i+1] - cu_seqlens_k[i] when seq_lens is NULL); sq_i <= sk_i.  Row r
  * is the query at absolute position p = sk_i - sq_i + r and attends keys
  * [max(0, p - w + 1), p] (all keys <= p without a window).  sq_i == 1 rows are
- * legal, so a mixed prefill + decode batch may be passed as one call.
+ * legal, so a mixed prefill + decode batch may be passed as one call; when seq_lens is
+ * given, those sequences run on the decode kernel within the call (no workspace needed)
+ * while the tensor-core kernel takes the rest.
  *
  *   out           [total_q, num_heads, head_dim] bf16, device (written)
  *   q             [total_q, num_heads, head_dim] bf16, device, 16-byte aligned
