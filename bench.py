@@ -39,8 +39,8 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # DRAM bytes (read + write) of one launch on the default workloads, from the ncu
 # captures summarised in profiles/ (commands there); None once a kernel changes.
 NCU_TRAFFIC = {
-    "decode_split_kernel": 639.78e6 + 5.64e6,
-    "prefill_kernel": 318.97e6 + 105.51e6,
+    "decode_split_kernel": 639.55e6 + 4.18e6,
+    "prefill_kernel": 314.22e6 + 104.51e6,
 }
 
 
