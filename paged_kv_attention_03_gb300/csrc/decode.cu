@@ -696,10 +696,18 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
 template <int D, int NWARPS, int NSTAGES, bool FP8>
 __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
     decode_split_body<D, NWARPS, NSTAGES, FP8>(p);
-    // The single-row (varlen) mode runs as a programmatic dependent of the prefill kernel
-    // of the same call: no CTA finishes before the prefill grid, so work queued later on
-    // the stream stays ordered after both.
-    if (p.after_prefill) sm100::griddep_wait();
+    // As a programmatic dependent of the prefill kernel of the same call (single-row
+    // sequences of a varlen batch, or a cascade's suffix) the CTAs run beside the prefill
+    // on the SMs it leaves free.  The grid's last CTA waits for the prefill grid, so this
+    // grid, the combine that waits for it and work queued later on the stream all
+    // complete after the prefill.
+    // (The CTA index is read again here, not kept live across the body.)
+    if (p.after_prefill) {
+        uint32_t x, y, z;
+        asm volatile("mov.u32 %0, %%ctaid.x;\n\tmov.u32 %1, %%ctaid.y;\n\tmov.u32 %2, %%ctaid.z;"
+                     : "=r"(x), "=r"(y), "=r"(z));
+        if (x == gridDim.x - 1 && y == gridDim.y - 1 && z == gridDim.z - 1) sm100::griddep_wait();
+    }
 }
 
 // Log-sum-exp merge of the splits of one (sequence, head) per warp:
@@ -824,9 +832,9 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     if (e != cudaSuccess) return e;
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
     if (kp.after_prefill) {
-        // After the prefill kernel, as its programmatic dependent: the CTAs take SMs as
-        // the prefill's persistent CTAs finish (the rows are disjoint; the cache writes
-        // they read were done by the store launch before the prefill).
+        // After the prefill kernel, as its programmatic dependent: the CTAs take the SMs
+        // the prefill leaves free (the output rows are disjoint; the cache rows they read
+        // were written by the store launch before the prefill).
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(kDecodeWarps * 32);

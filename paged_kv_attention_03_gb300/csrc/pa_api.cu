@@ -424,6 +424,8 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *k_cache, const
     a.pre_o = states;
     a.pre_lse = lses;
     a.pre_parts = c.n_splits;
+    // The suffix runs beside the prefix kernel, on the SMs its items leave free.
+    a.after_prefill = c.n_splits > 0;
     a.err = err;
     return from_cuda(pa::launch_decode(a, plan, s));
 }

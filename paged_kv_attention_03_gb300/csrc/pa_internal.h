@@ -84,7 +84,8 @@ struct DecodeArgs {
     const int32_t *q_rows;
     // Launch the split kernel as a programmatic dependent of the kernel before it (set
     // only right after the prefill kernel of the same call, which triggers its dependents
-    // once all its CTAs are resident; every split CTA then waits for that grid at exit).
+    // once all its CTAs are resident).  The split CTAs run beside the prefill; the grid's
+    // last CTA waits for the prefill grid before it exits.
     bool after_prefill;
     unsigned *err;
 };

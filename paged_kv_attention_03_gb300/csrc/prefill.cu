@@ -147,6 +147,7 @@ struct Layout {
     static constexpr uint32_t BYTES = OFF_INFO + kRing * 64;
     // At least 116 KB so a single CTA owns an SM (and all of its TMEM).
     static constexpr uint32_t SMEM = (BYTES + 1024 > 118784u ? BYTES + 1024 : 118784u);
+    static_assert(SMEM <= 232448u, "at most 227 KB of shared memory per CTA");
 };
 
 // Geometry of one work item; every role derives it identically.
@@ -361,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // Every CTA is resident: a programmatic dependent launched after this kernel (the
-    // single-row decode of the same call) may start taking SMs as CTAs finish.
+    // single-row decode of the same call, or the suffix decode of a cascade) may start
+    // on the SMs this grid leaves free.
     griddep_launch_dependents();
     const int bs_mask = (1 << p.log2_bs) - 1;
 
@@ -415,9 +417,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             // i mod P.  Items are published up to kAhead beyond the last Q load, so the K
             // and V producers can run ahead across short items.
             if (lane == 0) prefetch_tmap(&p.tmap_q);
-            const uint32_t P = gridDim.x, cta = blockIdx.x;
+            uint32_t P = gridDim.x;
+            const uint32_t cta = blockIdx.x;
             const int Hkv = p.num_kv_heads;
-            const int n_pairs = p.n_items / Hkv;  // (query block, sequence) pairs
+            int n_pairs = p.n_items / Hkv;  // (query block, sequence) pairs
+            if (!PREFIX && p.skip_decode_rows) {
+                // A batch whose single-row sequences go to the decode launch of the same
+                // call deals its items to only as many CTAs as the same number of rounds
+                // needs; the decode launch (a programmatic dependent of this kernel) takes
+                // the SMs of the others, which find no item and exit.  Every CTA counts the
+                // same sequences, so all agree on P.
+                uint32_t pairs = 0, rows1 = 0;
+                for (int i = lane; i < p.num_seqs; i += 32) {
+                    const int sq = p.cu_q[i + 1] - p.cu_q[i];
+                    if (sq == 1)
+                        ++rows1;
+                    else if (sq > 1)
+                        pairs += static_cast<uint32_t>(min((sq + 2 * T - 1) / (2 * T), p.q_items));
+                }
+                pairs = __reduce_add_sync(0xffffffffu, pairs);
+                rows1 = __reduce_add_sync(0xffffffffu, rows1);
+                const uint32_t v = pairs * static_cast<uint32_t>(Hkv);
+                if (rows1 != 0) {
+                    const uint32_t rounds = (v + P - 1) / P;
+                    P = v == 0 ? 1u : (v + rounds - 1) / rounds;
+                }
+                if (cta >= P) n_pairs = 0;
+            }
             // Target slot of round r: the snake order.
             auto target = [&](uint32_t r) -> uint32_t { return r * P + ((r & 1u) ? P - 1u - cta : cta); };
             uint32_t pub = 0, loaded = 0;  // items published / whose Q is loaded

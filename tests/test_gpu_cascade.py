@@ -67,3 +67,11 @@ def test_cascade_prefix_zero_and_prefix_only_requests(cuda):
     # A request whose every key is in the prefix (its suffix part is empty).
     case2, P2 = _shared_case(cuda, 32, 8, 128, 8, [0, 40, 3], seed=94)
     _check(case2, cuda, P2)
+
+
+def test_cascade_long_prefix_short_suffixes(cuda):
+    # An 8192-key shared prefix and suffixes of 1..8 keys: the suffix decode runs beside
+    # the prefix kernel and finishes first, so the merge must still wait for the prefix.
+    rng = np.random.default_rng(95)
+    case, P = _shared_case(cuda, 32, 8, 128, 512, rng.integers(1, 9, size=32), seed=95)
+    _check(case, cuda, P)

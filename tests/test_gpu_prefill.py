@@ -213,3 +213,18 @@ def test_prefill_full_size_mixed_chunks(cuda):
     case = make_case("mixed_window", seed=0, device=cuda)
     pre, dec = split_mixed(case)
     _sampled_rows_check(case, cuda, [pre[0], pre[3], pre[-1], dec[0], dec[-1]], n_rows=12)
+
+
+def test_mixed_call_orders_later_stream_work_after_the_prefill(cuda):
+    # Eight long prompts beside one decode row: the decode launch runs on the SMs the
+    # prefill leaves free and finishes long before it, yet work queued on the stream after
+    # the call (here a copy of the output) must see every prefill row.
+    w = Workload("order", 32, 8, 128, 16, ())
+    case = make_case_from_lengths(w, [0] * 8 + [300], [2048] * 8 + [1], seed=54, device=cuda)
+    out = torch.full_like(case.q, float("nan"))
+    _prefill(case, cuda, out=out)
+    snap = out.clone()  # same stream, no synchronisation before it
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error(device=cuda) == 0
+    assert not torch.isnan(out).any()
+    assert torch.equal(snap.view(torch.int16), out.view(torch.int16))
