@@ -186,16 +186,12 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
     constexpr int CPR = D / 8;                // 16-byte chunks per row
-    constexpr int ROWS_PER_PASS = 32 / CPR;
-    constexpr int PASSES = 16 / ROWS_PER_PASS;
     constexpr int KSTEPS = D / 16;
     constexpr int DTILES = D / 8;
     // FP8 ring: 16-key tiles of D bytes per row, twice as many stages in the same space.
     constexpr int TILE8 = 16 * D;
     constexpr int STAGE8 = 2 * TILE8;
     constexpr int CPR8 = D / 16;  // 16-byte chunks per fp8 row
-    constexpr int RPP8 = 32 / CPR8;
-    constexpr int PASSES8 = 16 / RPP8;
     constexpr int NST = FP8 ? 2 * NSTAGES : NSTAGES;  // ring depth
     constexpr int SB = FP8 ? STAGE8 : STAGE_BYTES;     // bytes per stage
     static_assert(NST * SB <= NSTAGES * STAGE_BYTES, "the ring fits the per-warp share");
@@ -354,90 +350,84 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     // With block_size >= 16 a 16-key unit never straddles two blocks: one table lookup
     // per unit and fixed row strides.  Smaller blocks take the per-row path.
     const bool page_units = p.log2_bs >= 4;
-    const int64_t row_stride = static_cast<int64_t>(p.num_kv_heads) * D;
 
     // The block of 16-key unit u (block_size >= 16: one lookup per unit).
     auto unit_block = [&](int u) -> int {
         return u == spec_unit ? spec_blk : __ldg(bt_row + ((u << 4) >> p.log2_bs));
     };
+    // Copy geometry of one 16-key unit: rows of RB bytes (one kv head), 16-byte chunks,
+    // RPP rows per pass of the warp.  Lane (c, rsub) copies chunk c of rows
+    // i * RPP + rsub; its byte offset within the unit is fixed, so each unit needs one
+    // 64-bit base and each pass one 32-bit add.
+    constexpr int RB = FP8 ? D : ROWB;
+    constexpr int CPRU = RB / 16;
+    constexpr int RPP = 32 / CPRU;
+    constexpr int NPASS = 16 / RPP;
+    constexpr int UT = 16 * RB;  // bytes of a K (or V) tile of one unit in shared memory
+    const uint8_t *kc8 = FP8 ? p.k8 : reinterpret_cast<const uint8_t *>(p.k_cache);
+    const uint8_t *vc8 = FP8 ? p.v8 : reinterpret_cast<const uint8_t *>(p.v_cache);
+    const int u_c = lane % CPRU;
+    const int u_rsub = lane / CPRU;
+    const int row_bytes = p.num_kv_heads * RB;
+    const int lane_off = u_rsub * row_bytes + kvh * RB + u_c * 16;
+    auto swz = [&](int c, int r) -> int {
+        if constexpr (FP8) return swz8<D>(c, r);
+        else return c ^ (r & 7);
+    };
     auto issue = [&](int u, int st) {
-        if constexpr (FP8) {
-            // fp8 rows of D bytes, 16-byte chunks, swizzled (swz8).
-            const uint32_t sb = stage_base + st * STAGE8;
-            const int c = lane % CPR8;
-            const int rsub = lane / CPR8;
-            const int j0 = u * 16;
-            int blk0 = 0;
-            bool blk0_ok = false;
-            if (page_units) {
-                blk0 = unit_block(u);
-                blk0_ok = blk0 >= 0 && blk0 < p.num_blocks;
-            }
-#pragma unroll
-            for (int i = 0; i < PASSES8; ++i) {
-                const int r = i * RPP8 + rsub;
-                const int j = j0 + r;
-                int64_t off = 0;
-                uint32_t nbytes = 0;
-                if (j >= lo && j < hi) {
-                    const int blk = page_units ? blk0 : __ldg(bt_row + (j >> p.log2_bs));
-                    if (page_units ? !blk0_ok : (blk < 0 || blk >= p.num_blocks)) {
-                        flag_error(p.err, kErrBlockRange);
-                    } else {
-                        off = (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
-                                   p.num_kv_heads + kvh) * D + c * 16;
-                        nbytes = 16;
-                    }
-                }
-                const uint32_t so = r * D + (swz8<D>(c, r) << 4);
-                cp_async_16_policy(sb + so, p.k8 + off, nbytes, policy);
-                cp_async_16_policy(sb + TILE8 + so, p.v8 + off, nbytes, policy);
-            }
-            return;
-        }
-        const uint32_t sb = stage_base + st * STAGE_BYTES;
-        const int c = lane % CPR;
-        const int rsub = lane / CPR;
+        const uint32_t sb = stage_base + st * SB;
         const int j0 = u * 16;
         if (page_units) {
-            const bool full = j0 >= lo && j0 + 16 <= hi;
             const int blk = unit_block(u);
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             if (!blk_ok && lane == 0) flag_error(p.err, kErrBlockRange);
-            const int64_t base =
-                blk_ok ? (((static_cast<int64_t>(blk) << p.log2_bs) + (j0 & bs_mask)) *
-                              p.num_kv_heads + kvh) * D + c * 8
+            const int64_t uoff =
+                blk_ok ? ((static_cast<int64_t>(blk) << p.log2_bs) + (j0 & bs_mask)) * row_bytes +
+                             lane_off
                        : 0;
+            const uint8_t *ks = kc8 + uoff;
+            const uint8_t *vs = vc8 + uoff;
+            if (blk_ok && j0 >= lo && j0 + 16 <= hi) {  // a full unit: no row checks
 #pragma unroll
-            for (int i = 0; i < PASSES; ++i) {
-                const int r = i * ROWS_PER_PASS + rsub;
-                const bool ok = blk_ok && (full || (j0 + r >= lo && j0 + r < hi));
-                const int64_t off = ok ? base + r * row_stride : 0;
-                const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
-                cp_async_16_policy(sb + so, p.k_cache + off, ok ? 16u : 0u, policy);
-                cp_async_16_policy(sb + TILE_BYTES + so, p.v_cache + off, ok ? 16u : 0u, policy);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < PASSES; ++i) {
-                const int r = i * ROWS_PER_PASS + rsub;
-                const int j = j0 + r;
-                int64_t off = 0;
-                uint32_t nbytes = 0;
-                if (j >= lo && j < hi) {
-                    const int blk = __ldg(bt_row + (j >> p.log2_bs));
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        flag_error(p.err, kErrBlockRange);
-                    } else {
-                        off = (((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) *
-                                   p.num_kv_heads + kvh) * D + c * 8;
-                        nbytes = 16;
-                    }
+                for (int i = 0; i < NPASS; ++i) {
+                    const int r = i * RPP + u_rsub;
+                    const uint32_t so = r * RB + (swz(u_c, r) << 4);
+                    cp_async_16_policy(sb + so, ks + i * RPP * row_bytes, 16u, policy);
+                    cp_async_16_policy(sb + UT + so, vs + i * RPP * row_bytes, 16u, policy);
                 }
-                const uint32_t so = r * ROWB + ((c ^ (r & 7)) << 4);
-                cp_async_16_policy(sb + so, p.k_cache + off, nbytes, policy);
-                cp_async_16_policy(sb + TILE_BYTES + so, p.v_cache + off, nbytes, policy);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NPASS; ++i) {
+                    const int r = i * RPP + u_rsub;
+                    const bool ok = blk_ok && j0 + r >= lo && j0 + r < hi;
+                    const int o = ok ? i * RPP * row_bytes : 0;
+                    const uint32_t so = r * RB + (swz(u_c, r) << 4);
+                    cp_async_16_policy(sb + so, ok ? ks + o : kc8, ok ? 16u : 0u, policy);
+                    cp_async_16_policy(sb + UT + so, ok ? vs + o : vc8, ok ? 16u : 0u, policy);
+                }
             }
+            return;
+        }
+        // block_size < 16: one table lookup per row.
+#pragma unroll
+        for (int i = 0; i < NPASS; ++i) {
+            const int r = i * RPP + u_rsub;
+            const int j = j0 + r;
+            int64_t off = 0;
+            uint32_t nbytes = 0;
+            if (j >= lo && j < hi) {
+                const int blk = __ldg(bt_row + (j >> p.log2_bs));
+                if (blk < 0 || blk >= p.num_blocks) {
+                    flag_error(p.err, kErrBlockRange);
+                } else {
+                    off = ((static_cast<int64_t>(blk) << p.log2_bs) + (j & bs_mask)) * row_bytes +
+                          lane_off - u_rsub * row_bytes;
+                    nbytes = 16;
+                }
+            }
+            const uint32_t so = r * RB + (swz(u_c, r) << 4);
+            cp_async_16_policy(sb + so, kc8 + off, nbytes, policy);
+            cp_async_16_policy(sb + UT + so, vc8 + off, nbytes, policy);
         }
     };
 
