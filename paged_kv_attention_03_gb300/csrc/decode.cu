@@ -123,18 +123,37 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-// Two FP8 E4M3 codes (low byte first) -> f16x2, exactly: every E4M3 value (at most 4
-// significant bits, exponents 2^-9 .. 2^8) is an f16.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    uint32_t h;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
-    return h;
+// Four FP8 E4M3 codes (low byte first) -> two f16x2 words, exactly (every E4M3 value, at
+// most 4 significant bits with exponents 2^-9 .. 2^8, is an f16): codes 0, 1 into lo and
+// codes 2, 3 into hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    asm("{\n"
+        ".reg .b16 a, b;\n"
+        "mov.b32 {a, b}, %2;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n"
+        "}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t h;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
     return h;
+}
+
+// acc += float(bf16 low half of v) + float(bf16 high half of v) (mixed-precision adds:
+// the bf16 halves go in directly, exactly).
+__device__ __forceinline__ void add_bf16x2_f32(float &acc, uint32_t v) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %1;\n"
+        "add.rn.f32.bf16 %0, l, %0;\n"
+        "add.rn.f32.bf16 %0, h, %0;\n"
+        "}\n"
+        : "+f"(acc)
+        : "r"(v));
 }
 
 // acc += float(f16 low half of v) + float(f16 high half of v) (mixed-precision adds).
@@ -474,12 +493,13 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
             for (int kq = 0; kq < D / 32; ++kq) {
                 uint32_t kw[4];
                 ldmatrix_x4(kw, kb + r * D + (swz8<D>(2 * kq + chi, r) << 4));
-                mma_f16_16816(s[0], qa[2 * kq], e4m3x2_to_f16x2(kw[0]), e4m3x2_to_f16x2(kw[0] >> 16));
-                mma_f16_16816(s[1], qa[2 * kq], e4m3x2_to_f16x2(kw[2]), e4m3x2_to_f16x2(kw[2] >> 16));
-                mma_f16_16816(s2[0], qa[2 * kq + 1], e4m3x2_to_f16x2(kw[1]),
-                              e4m3x2_to_f16x2(kw[1] >> 16));
-                mma_f16_16816(s2[1], qa[2 * kq + 1], e4m3x2_to_f16x2(kw[3]),
-                              e4m3x2_to_f16x2(kw[3] >> 16));
+                uint32_t kf[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(kw[i], kf[i][0], kf[i][1]);
+                mma_f16_16816(s[0], qa[2 * kq], kf[0][0], kf[0][1]);
+                mma_f16_16816(s[1], qa[2 * kq], kf[2][0], kf[2][1]);
+                mma_f16_16816(s2[0], qa[2 * kq + 1], kf[1][0], kf[1][1]);
+                mma_f16_16816(s2[1], qa[2 * kq + 1], kf[3][0], kf[3][1]);
             }
         } else {
             const int r = ((lane >> 4) << 3) + (lane & 7);
@@ -566,10 +586,10 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
             pa[1] = pack_bf16x2(s[0][2], s[0][3]);
             pa[2] = pack_bf16x2(s[1][0], s[1][1]);
             pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-            l_run[0] += __uint_as_float(pa[0] << 16) + __uint_as_float(pa[0] & 0xffff0000u) +
-                        __uint_as_float(pa[2] << 16) + __uint_as_float(pa[2] & 0xffff0000u);
-            l_run[1] += __uint_as_float(pa[1] << 16) + __uint_as_float(pa[1] & 0xffff0000u) +
-                        __uint_as_float(pa[3] << 16) + __uint_as_float(pa[3] & 0xffff0000u);
+            add_bf16x2_f32(l_run[0], pa[0]);
+            add_bf16x2_f32(l_run[0], pa[2]);
+            add_bf16x2_f32(l_run[1], pa[1]);
+            add_bf16x2_f32(l_run[1], pa[3]);
         }
 
         // O += P V.
@@ -587,9 +607,11 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t x0 = __byte_perm(vw[2 * h], 0u, 0x3120);      // keys 0-7
                     const uint32_t x1 = __byte_perm(vw[2 * h + 1], 0u, 0x3120);  // keys 8-15
-                    mma_f16_16816(o[4 * dq + 2 * h], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
-                    mma_f16_16816(o[4 * dq + 2 * h + 1], pa, e4m3x2_to_f16x2(x0 >> 16),
-                                  e4m3x2_to_f16x2(x1 >> 16));
+                    uint32_t f0[2], f1[2];  // [even dim, odd dim]
+                    e4m3x4_to_f16x2x2(x0, f0[0], f0[1]);
+                    e4m3x4_to_f16x2x2(x1, f1[0], f1[1]);
+                    mma_f16_16816(o[4 * dq + 2 * h], pa, f0[0], f1[0]);
+                    mma_f16_16816(o[4 * dq + 2 * h + 1], pa, f0[1], f1[1]);
                 }
             }
         } else {
