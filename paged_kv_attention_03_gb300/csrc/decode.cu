@@ -156,6 +156,27 @@ __device__ __forceinline__ void add_bf16x2_f32(float &acc, uint32_t v) {
         : "r"(v));
 }
 
+// lo += float(f16 low half of v), hi += float(f16 high half of v) (mixed-precision adds).
+__device__ __forceinline__ void add_f16x2_f32(float &lo, float &hi, uint32_t v) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %2;\n"
+        "add.rn.f32.f16 %0, l, %0;\n"
+        "add.rn.f32.f16 %1, h, %1;\n"
+        "}\n"
+        : "+f"(lo), "+f"(hi)
+        : "r"(v));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as the MMA accumulator fragment
+// (lane holds row lane/4, columns 2 (lane%4) and + 1): afterwards the lane holds row
+// lane/4 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // acc += float(f16 low half of v) + float(f16 high half of v) (mixed-precision adds).
 __device__ __forceinline__ void add_f16x2_f32(float &acc, uint32_t v) {
     asm("{\n"
@@ -199,7 +220,7 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // fp8 rows with the head-dim index permuted alike in Q, V fragments from a transposing
 // ldmatrix on byte pairs plus one byte permute (even and odd head dims in separate
 // MMAs).  kv_scale is applied to the scores (K) and the results (V); Q and P are f16.
-template <int D, int NWARPS, int NSTAGES, bool FP8>
+template <int D, int NWARPS, int NSTAGES, bool FP8, int NT>
 __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     constexpr int ROWB = D * 2;               // bytes of one key row of one kv head
     constexpr int TILE_BYTES = 16 * ROWB;     // 16 keys
@@ -320,15 +341,17 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
         return;
     }
 
-    // Q fragments (A operand, 16 rows = query heads of this tile, zero padded).
-    uint32_t qa[KSTEPS][4];
+    // Q^T fragments: the B operand (k = head dims, n = heads) of S^T = K Q^T, per n-tile j
+    // of 8 heads (head 8 j + lane / 4) and 16-dim k-step ks: two 32-bit words.  Heads past
+    // the group are zero.
+    uint32_t qf[NT][KSTEPS][2];
     {
         const __nv_bfloat16 *qb = p.q + (static_cast<int64_t>(qrow) * p.num_heads + h0) * D;
-        const int r0 = lane >> 2;
+        const int g = lane >> 2;
         if constexpr (FP8) {
-            // f16, head dims permuted as the K fragments deliver them: MMA k 2j, 2j+1 are
-            // dims 4j, 4j+1 and k 2j+8, 2j+9 are dims 4j+2, 4j+3 of the 16-dim step
-            // (j = lane % 4).  |q| is clamped to the f16 range.
+            // f16, with the k order of the K fragments: k 2t, 2t+1 are dims 4t, 4t+1 and
+            // k 2t+8, 2t+9 dims 4t+2, 4t+3 of the step (t = lane % 4).  |q| is clamped
+            // to the f16 range.
             const int c0 = (lane & 3) * 4;
             auto f16pair = [](uint32_t w) -> uint32_t {
                 const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
@@ -336,25 +359,25 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
                 return pack_f16x2(lo, hi);
             };
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                uint2 x0 = make_uint2(0u, 0u), x1 = make_uint2(0u, 0u);
-                if (r0 < rows_valid) x0 = *reinterpret_cast<const uint2 *>(qb + r0 * D + ks * 16 + c0);
-                if (r0 + 8 < rows_valid)
-                    x1 = *reinterpret_cast<const uint2 *>(qb + (r0 + 8) * D + ks * 16 + c0);
-                qa[ks][0] = f16pair(x0.x);
-                qa[ks][1] = f16pair(x1.x);
-                qa[ks][2] = f16pair(x0.y);
-                qa[ks][3] = f16pair(x1.y);
-            }
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    uint2 x = make_uint2(0u, 0u);
+                    if (8 * j + g < rows_valid)
+                        x = *reinterpret_cast<const uint2 *>(qb + (8 * j + g) * D + ks * 16 + c0);
+                    qf[j][ks][0] = f16pair(x.x);
+                    qf[j][ks][1] = f16pair(x.y);
+                }
         } else {
             const int c0 = (lane & 3) * 2;
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                qa[ks][0] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0) : 0u;
-                qa[ks][1] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0) : 0u;
-                qa[ks][2] = r0 < rows_valid ? ld_u32(qb + r0 * D + ks * 16 + c0 + 8) : 0u;
-                qa[ks][3] = r0 + 8 < rows_valid ? ld_u32(qb + (r0 + 8) * D + ks * 16 + c0 + 8) : 0u;
-            }
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const bool ok = 8 * j + g < rows_valid;
+                    qf[j][ks][0] = ok ? ld_u32(qb + (8 * j + g) * D + ks * 16 + c0) : 0u;
+                    qf[j][ks][1] = ok ? ld_u32(qb + (8 * j + g) * D + ks * 16 + c0 + 8) : 0u;
+                }
         }
     }
 
@@ -450,13 +473,23 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
         }
     };
 
-    float o[DTILES][4];
+    // O^T accumulators: m-tile mt of 16 head dims x n-tile j of 8 heads.  bf16: rows are
+    // dims 16 mt + lane / 4 (+ 8); FP8 (mt = 2 dq + e): dims 32 dq + 2 (lane / 4) + e (+ 16).
+    // Columns (heads) 8 j + 2 (lane % 4) and + 1.
+    float o[NT][DTILES / 2][4];
 #pragma unroll
-    for (int i = 0; i < DTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // m_run is the reference maximum the weights are taken against: it only moves when
-    // the true maximum exceeds it by more than 2^8, so O is rarely rescaled.
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int i = 0; i < DTILES / 2; ++i) o[j][i][0] = o[j][i][1] = o[j][i][2] = o[j][i][3] = 0.f;
+    // Per head (8 j + 2 (lane % 4) + e): m_run is the reference maximum the weights are
+    // taken against; it only moves when the true maximum exceeds it by more than 2^8, so O
+    // is rarely rescaled.  l_run sums this lane's keys; lanes are summed at the end.
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+    }
 
     const int my_first = u_first + warp;
     // Prologue: NST - 1 units in flight.
@@ -466,6 +499,15 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
         if (u <= u_last) issue(u, st);
         cp_async_commit();
     }
+
+    const int g = lane >> 2;
+    // ldmatrix row addresses.  K (A operand, non-transposed): matrices (keys 0-7, chunk c),
+    // (keys 8-15, c), (keys 0-7, c + 1), (keys 8-15, c + 1).  V (A operand of O^T,
+    // transposed): (keys 0-7, c), (keys 0-7, c + 1), (keys 8-15, c), (keys 8-15, c + 1).
+    const int rk = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int ck = lane >> 4;
+    const int rv = (lane >> 4) * 8 + (lane & 7);
+    const int cv = (lane >> 3) & 1;
 
     int it = 0;
     for (int u = my_first; u <= u_last; u += NWARPS, ++it) {
@@ -478,152 +520,149 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
         __syncwarp();
 
         const uint32_t kb = stage_base + (it % NST) * SB;
-        const uint32_t vb = kb + (FP8 ? TILE8 : TILE_BYTES);
+        const uint32_t vb = kb + UT;
 
-        // S = Q K^T for 16 keys: two n-tiles of 8 keys, even and odd k-steps in
+        // S^T = K Q^T for 16 keys (M) and 8 heads per n-tile (N); even and odd k-steps in
         // separate accumulators to halve the dependent MMA chain.
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float s[NT][4], s2[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[j][e] = s2[j][e] = 0.f;
         if constexpr (FP8) {
-            // One ldmatrix.x4 covers 16 keys x 32 head dims (two k-steps); each 32-bit
-            // word holds 4 consecutive dims of one key: two f16 pairs, b0 and b1.
-            const int r = ((lane >> 4) << 3) + (lane & 7);
-            const int chi = (lane >> 3) & 1;
+            // One ldmatrix.x4 covers 16 keys x 32 dims (two k-steps); a word holds 4
+            // consecutive dims of one key: its low f16 pair is k 2t, 2t+1 and its high pair
+            // k 2t+8, 2t+9 of the step.
 #pragma unroll
             for (int kq = 0; kq < D / 32; ++kq) {
                 uint32_t kw[4];
-                ldmatrix_x4(kw, kb + r * D + (swz8<D>(2 * kq + chi, r) << 4));
-                uint32_t kf[4][2];
+                ldmatrix_x4(kw, kb + rk * D + (swz8<D>(2 * kq + ck, rk) << 4));
+                uint32_t f[4][2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(kw[i], kf[i][0], kf[i][1]);
-                mma_f16_16816(s[0], qa[2 * kq], kf[0][0], kf[0][1]);
-                mma_f16_16816(s[1], qa[2 * kq], kf[2][0], kf[2][1]);
-                mma_f16_16816(s2[0], qa[2 * kq + 1], kf[1][0], kf[1][1]);
-                mma_f16_16816(s2[1], qa[2 * kq + 1], kf[3][0], kf[3][1]);
+                for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(kw[i], f[i][0], f[i][1]);
+                const uint32_t a0[4] = {f[0][0], f[1][0], f[0][1], f[1][1]};
+                const uint32_t a1[4] = {f[2][0], f[3][0], f[2][1], f[3][1]};
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    mma_f16_16816(s[j], a0, qf[j][2 * kq][0], qf[j][2 * kq][1]);
+                    mma_f16_16816(s2[j], a1, qf[j][2 * kq + 1][0], qf[j][2 * kq + 1][1]);
+                }
             }
         } else {
-            const int r = ((lane >> 4) << 3) + (lane & 7);
-            const int chi = (lane >> 3) & 1;
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                uint32_t kf[4];
-                const int ch = 2 * ks + chi;
-                ldmatrix_x4(kf, kb + r * ROWB + ((ch ^ (r & 7)) << 4));
-                if (ks & 1) {
-                    mma_bf16_16816(s2[0], qa[ks], kf[0], kf[1]);
-                    mma_bf16_16816(s2[1], qa[ks], kf[2], kf[3]);
-                } else {
-                    mma_bf16_16816(s[0], qa[ks], kf[0], kf[1]);
-                    mma_bf16_16816(s[1], qa[ks], kf[2], kf[3]);
-                }
+                uint32_t ka[4];
+                ldmatrix_x4(ka, kb + rk * ROWB + (((2 * ks + ck) ^ (rk & 7)) << 4));
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                    mma_bf16_16816((ks & 1) ? s2[j] : s[j], ka, qf[j][ks][0], qf[j][ks][1]);
             }
         }
 
-        // Scale, mask (edge units only), online softmax on rows lane/4 and lane/4 + 8.
+        // Scale, mask (edge units only), online softmax per head column: elements 0, 1 are
+        // key u*16 + lane/4, elements 2, 3 key + 8; elements 0, 2 head 2t, 1, 3 head 2t+1.
         const bool edge = u * 16 < lo || u * 16 + 16 > hi;
-        float mx[2] = {-INFINITY, -INFINITY};
+        float mx[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int j = 0; j < NT; ++j) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float v = (s[nt][e] + s2[nt][e]) * p.scale_log2;
+                float v = (s[j][e] + s2[j][e]) * p.scale_log2;
                 if (edge) {
-                    const int j = u * 16 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                    if (j < lo || j >= hi) v = -INFINITY;
+                    const int key = u * 16 + g + (e >> 1) * 8;
+                    if (key < lo || key >= hi) v = -INFINITY;
                 }
-                s[nt][e] = v;
-                mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                s[j][e] = v;
+            }
+            mx[j][0] = fmaxf(s[j][0], s[j][2]);
+            mx[j][1] = fmaxf(s[j][1], s[j][3]);
+        }
+        bool need = false;
+        float m_new[NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float m = mx[j][e];
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                m_new[j][e] = fmaxf(m_run[j][e], m);
+                need |= m_new[j][e] > m_run[j][e] + 8.f;
+            }
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float f[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const bool nd = m_new[j][e] > m_run[j][e] + 8.f;
+                    f[e] = nd ? ex2_approx(m_run[j][e] - m_new[j][e]) : 1.f;
+                    l_run[j][e] *= f[e];
+                    if (nd) m_run[j][e] = m_new[j][e];
+                }
+#pragma unroll
+                for (int mt = 0; mt < DTILES / 2; ++mt) {
+                    o[j][mt][0] *= f[0];
+                    o[j][mt][1] *= f[1];
+                    o[j][mt][2] *= f[0];
+                    o[j][mt][3] *= f[1];
+                }
             }
         }
-        bool need[2];
-        float m_new[2];
+        // P^T (B operand of O^T = V^T P^T): the weights packed per key row (heads 2t, 2t+1)
+        // and transposed by movmatrix into (head lane/4; keys 2t, 2t+1) words.  The
+        // denominator sums the rounded weights the MMA actually uses.
+        uint32_t pb[NT][2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-            m_new[i] = fmaxf(m_run[i], mx[i]);
-            need[i] = m_new[i] > m_run[i] + 8.f;
-        }
-        if (__any_sync(0xffffffffu, need[0] || need[1])) {
-            float f[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                f[i] = need[i] ? ex2_approx(m_run[i] - m_new[i]) : 1.f;
-                l_run[i] *= f[i];
-                if (need[i]) m_run[i] = m_new[i];
+        for (int j = 0; j < NT; ++j) {
+            const float m0 = m_run[j][0] == -INFINITY ? 0.f : m_run[j][0];
+            const float m1 = m_run[j][1] == -INFINITY ? 0.f : m_run[j][1];
+            const float e0 = ex2_approx(s[j][0] - m0), e1 = ex2_approx(s[j][1] - m1);
+            const float e2 = ex2_approx(s[j][2] - m0), e3 = ex2_approx(s[j][3] - m1);
+            uint32_t w0, w1;
+            if constexpr (FP8) {
+                w0 = pack_f16x2(e0, e1);
+                w1 = pack_f16x2(e2, e3);
+                add_f16x2_f32(l_run[j][0], l_run[j][1], w0);
+                add_f16x2_f32(l_run[j][0], l_run[j][1], w1);
+            } else {
+                w0 = pack_bf16x2(e0, e1);
+                w1 = pack_bf16x2(e2, e3);
+                sm100::add_bf16x2_f32(l_run[j][0], l_run[j][1], w0);
+                sm100::add_bf16x2_f32(l_run[j][0], l_run[j][1], w1);
             }
-#pragma unroll
-            for (int dt = 0; dt < DTILES; ++dt) {
-                o[dt][0] *= f[0];
-                o[dt][1] *= f[0];
-                o[dt][2] *= f[1];
-                o[dt][3] *= f[1];
-            }
-        }
-        const float m_use0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
-        const float m_use1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            s[nt][0] = ex2_approx(s[nt][0] - m_use0);
-            s[nt][1] = ex2_approx(s[nt][1] - m_use0);
-            s[nt][2] = ex2_approx(s[nt][2] - m_use1);
-            s[nt][3] = ex2_approx(s[nt][3] - m_use1);
-        }
-        // P as the A operand straight from the S accumulators (f16 for the FP8 cache);
-        // the denominator sums the rounded weights the MMA actually uses.
-        uint32_t pa[4];
-        if constexpr (FP8) {
-            pa[0] = pack_f16x2(s[0][0], s[0][1]);
-            pa[1] = pack_f16x2(s[0][2], s[0][3]);
-            pa[2] = pack_f16x2(s[1][0], s[1][1]);
-            pa[3] = pack_f16x2(s[1][2], s[1][3]);
-            add_f16x2_f32(l_run[0], pa[0]);
-            add_f16x2_f32(l_run[0], pa[2]);
-            add_f16x2_f32(l_run[1], pa[1]);
-            add_f16x2_f32(l_run[1], pa[3]);
-        } else {
-            pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-            pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-            pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-            pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-            add_bf16x2_f32(l_run[0], pa[0]);
-            add_bf16x2_f32(l_run[0], pa[2]);
-            add_bf16x2_f32(l_run[1], pa[1]);
-            add_bf16x2_f32(l_run[1], pa[3]);
+            pb[j][0] = movmatrix_trans(w0);  // keys 0-7
+            pb[j][1] = movmatrix_trans(w1);  // keys 8-15
         }
 
-        // O += P V.
+        // O^T += V^T P^T.
         if constexpr (FP8) {
-            // ldmatrix.trans on byte pairs: a word holds (key 2j, dims 2c', 2c'+1) and
-            // (key 2j+1, same dims); one byte permute makes the key pairs of dim 2c' and
-            // of dim 2c'+1.  o[4 dq + 2 h + e] holds dims 32 dq + 16 h + 2 n + e.
-            const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
-            const int chi = lane >> 4;
+            // ldmatrix.trans on byte pairs: a word holds (key 2t, dims 2c', 2c'+1) and
+            // (key 2t+1, same dims); one byte permute makes the key pairs of dim 2c' (low
+            // half) and of dim 2c'+1 (high half): even and odd dims are separate m-tiles.
 #pragma unroll
             for (int dq = 0; dq < D / 32; ++dq) {
                 uint32_t vw[4];
-                ldmatrix_x4_trans(vw, vb + r * D + (swz8<D>(2 * dq + chi, r) << 4));
+                ldmatrix_x4_trans(vw, vb + rv * D + (swz8<D>(2 * dq + cv, rv) << 4));
+                uint32_t f[4][2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t x0 = __byte_perm(vw[2 * h], 0u, 0x3120);      // keys 0-7
-                    const uint32_t x1 = __byte_perm(vw[2 * h + 1], 0u, 0x3120);  // keys 8-15
-                    uint32_t f0[2], f1[2];  // [even dim, odd dim]
-                    e4m3x4_to_f16x2x2(x0, f0[0], f0[1]);
-                    e4m3x4_to_f16x2x2(x1, f1[0], f1[1]);
-                    mma_f16_16816(o[4 * dq + 2 * h], pa, f0[0], f1[0]);
-                    mma_f16_16816(o[4 * dq + 2 * h + 1], pa, f0[1], f1[1]);
+                for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(__byte_perm(vw[i], 0u, 0x3120), f[i][0], f[i][1]);
+                const uint32_t ae[4] = {f[0][0], f[1][0], f[2][0], f[3][0]};
+                const uint32_t ao[4] = {f[0][1], f[1][1], f[2][1], f[3][1]};
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    mma_f16_16816(o[j][2 * dq], ae, pb[j][0], pb[j][1]);
+                    mma_f16_16816(o[j][2 * dq + 1], ao, pb[j][0], pb[j][1]);
                 }
             }
         } else {
-            const int r = (((lane >> 3) & 1) << 3) + (lane & 7);
-            const int chi = lane >> 4;
 #pragma unroll
             for (int dp = 0; dp < D / 16; ++dp) {
-                uint32_t vf[4];
-                const int ch = 2 * dp + chi;
-                ldmatrix_x4_trans(vf, vb + r * ROWB + ((ch ^ (r & 7)) << 4));
-                mma_bf16_16816(o[2 * dp], pa, vf[0], vf[1]);
-                mma_bf16_16816(o[2 * dp + 1], pa, vf[2], vf[3]);
+                uint32_t va[4];
+                ldmatrix_x4_trans(va, vb + rv * ROWB + (((2 * dp + cv) ^ (rv & 7)) << 4));
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma_bf16_16816(o[j][dp], va, pb[j][0], pb[j][1]);
             }
         }
         __syncwarp();
@@ -633,10 +672,13 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     sm100::griddep_launch_dependents();
 
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
-        l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
-    }
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l_run[j][e] += __shfl_xor_sync(0xffffffffu, l_run[j][e], 4);
+            l_run[j][e] += __shfl_xor_sync(0xffffffffu, l_run[j][e], 8);
+            l_run[j][e] += __shfl_xor_sync(0xffffffffu, l_run[j][e], 16);
+        }
 
     // Merge the warps of the CTA through shared memory (the stage ring is free now).
     __syncthreads();
@@ -645,31 +687,31 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     float *l_s = m_s + NWARPS * 16;
     float *o_s = l_s + NWARPS * 16;
     {
-        const int r0 = lane >> 2;
-        if ((lane & 3) == 0) {
-            m_s[warp * 16 + r0] = m_run[0];
-            m_s[warp * 16 + r0 + 8] = m_run[1];
-            l_s[warp * 16 + r0] = l_run[0];
-            l_s[warp * 16 + r0 + 8] = l_run[1];
-        }
-        float *ow = o_s + warp * 16 * OSTRIDE;
-        if constexpr (FP8) {
+        const int t = lane & 3;
 #pragma unroll
-            for (int dt = 0; dt < DTILES; ++dt) {
-                // dt = 4 dq + 2 h + e: dims 32 dq + 16 h + 4 (lane % 4) + e and + 2
-                const int d = (dt >> 2) * 32 + ((dt >> 1) & 1) * 16 + (lane & 3) * 4 + (dt & 1);
-                ow[r0 * OSTRIDE + d] = o[dt][0];
-                ow[r0 * OSTRIDE + d + 2] = o[dt][1];
-                ow[(r0 + 8) * OSTRIDE + d] = o[dt][2];
-                ow[(r0 + 8) * OSTRIDE + d + 2] = o[dt][3];
+        for (int j = 0; j < NT; ++j) {
+            if (g == 0) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    m_s[warp * 16 + 8 * j + 2 * t + e] = m_run[j][e];
+                    l_s[warp * 16 + 8 * j + 2 * t + e] = l_run[j][e];
+                }
             }
-        } else {
+            float *ow = o_s + (warp * 16 + 8 * j + 2 * t) * OSTRIDE;
 #pragma unroll
-            for (int dt = 0; dt < DTILES; ++dt) {
-                const int d = dt * 8 + (lane & 3) * 2;
-                *reinterpret_cast<float2 *>(ow + r0 * OSTRIDE + d) = make_float2(o[dt][0], o[dt][1]);
-                *reinterpret_cast<float2 *>(ow + (r0 + 8) * OSTRIDE + d) =
-                    make_float2(o[dt][2], o[dt][3]);
+            for (int mt = 0; mt < DTILES / 2; ++mt) {
+                int d0, d1;
+                if constexpr (FP8) {
+                    d0 = (mt >> 1) * 32 + 2 * g + (mt & 1);
+                    d1 = d0 + 16;
+                } else {
+                    d0 = mt * 16 + g;
+                    d1 = d0 + 8;
+                }
+                ow[d0] = o[j][mt][0];
+                ow[OSTRIDE + d0] = o[j][mt][1];
+                ow[d1] = o[j][mt][2];
+                ow[OSTRIDE + d1] = o[j][mt][3];
             }
         }
     }
@@ -705,9 +747,9 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     }
 }
 
-template <int D, int NWARPS, int NSTAGES, bool FP8>
+template <int D, int NWARPS, int NSTAGES, bool FP8, int NT>
 __global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
-    decode_split_body<D, NWARPS, NSTAGES, FP8>(p);
+    decode_split_body<D, NWARPS, NSTAGES, FP8, NT>(p);
     // As a programmatic dependent of the prefill kernel of the same call (single-row
     // sequences of a varlen batch, or a cascade's suffix) the CTAs run beside the prefill
     // on the SMs it leaves free.  The grid's last CTA waits for the prefill grid, so this
@@ -839,7 +881,9 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     constexpr int smem = decode_smem_bytes<D>();
     static_assert(smem >= (kDecodeWarps * 16 * 2 + kDecodeWarps * 16 * (D + 4)) * 4,
                   "merge area must fit in the stage ring");
-    auto kern = decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8>;
+    // 8 heads per n-tile: a group of at most 8 query heads takes one, larger ones two.
+    auto kern = kp.group <= 8 ? decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 1>
+                              : decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 2>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
