@@ -8,6 +8,7 @@ so.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -135,7 +136,15 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
+# The current stream's raw handle without building a Stream object (about 2 us less per
+# call); torch.cuda.current_stream is the fallback.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device: torch.device) -> int:
+    if _raw_stream is not None:
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        return _raw_stream(idx)
     return torch.cuda.current_stream(device).cuda_stream
 
 
@@ -231,6 +240,7 @@ def pa_decode_num_splits(batch: int, num_heads: int, num_kv_heads: int, head_dim
                                            max_seq_len, sliding_window, num_splits))
 
 
+@functools.lru_cache(maxsize=1024)
 def pa_decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
                              max_seq_len: int, sliding_window: int = 0,
                              num_splits: int = 0) -> int:

@@ -882,9 +882,11 @@ cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan
     static_assert(smem >= (kDecodeWarps * 16 * 2 + kDecodeWarps * 16 * (D + 4)) * 4,
                   "merge area must fit in the stage ring");
     // 8 heads per n-tile: a group of at most 8 query heads takes one, larger ones two.
-    auto kern = kp.group <= 8 ? decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 1>
-                              : decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 2>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> smem_set[2];
+    const int nt = kp.group <= 8 ? 0 : 1;
+    auto kern = nt == 0 ? decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 1>
+                        : decode_split_kernel<D, kDecodeWarps, kDecodeStages, FP8, 2>;
+    cudaError_t e = smem_limit_once(kern, smem, smem_set[nt]);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.num_splits, kp.num_kv_heads * plan.head_tiles, batch);
     if (kp.after_prefill) {

@@ -6,6 +6,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <cstdint>
+
 #include "pa_gb300.h"
 
 namespace pa {
@@ -160,5 +163,20 @@ cudaError_t launch_merge_states(const MergeArgs &a, cudaStream_t stream);
 
 // Map a CUDA error to a pa_status, remembering it for pa_last_cuda_error_string().
 pa_status cuda_status(cudaError_t e);
+
+// Raises kernel f's dynamic shared-memory limit to `bytes` once per device (done: one bit
+// per device ordinal, owned by the caller for that kernel), so launches after the first
+// make no attribute call.
+template <typename Kernel>
+inline cudaError_t smem_limit_once(Kernel f, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 }  // namespace pa

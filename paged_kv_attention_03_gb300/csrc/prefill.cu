@@ -1051,8 +1051,8 @@ cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cuda
                    HD * 2ull, static_cast<uint64_t>(a.num_kv_heads) * HD * 2ull, 64, 1, 16))
         return cudaErrorInvalidValue;
     auto kern = prefill_kernel<HD, PREFIX>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    static std::atomic<uint64_t> smem_set;
+    cudaError_t e = smem_limit_once(kern, static_cast<int>(L::SMEM), smem_set);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int grid = kp.n_items < sms ? kp.n_items : sms;
