@@ -80,7 +80,7 @@ def test_decode_block_sizes(cuda, bs):
 
 
 @pytest.mark.parametrize("H,Hkv,D", [(8, 8, 128), (40, 8, 128), (16, 1, 64), (20, 1, 128),
-                                     (64, 2, 64), (6, 3, 64)])
+                                     (64, 2, 64), (6, 3, 64), (24, 2, 128), (36, 4, 64)])
 def test_decode_group_sizes_and_head_dims(cuda, H, Hkv, D):
     w = Workload("g", H, Hkv, D, 16, ())
     case = make_case_from_lengths(w, [0, 1, 14, 15, 16, 17, 333], [1] * 7, seed=36, device=cuda)

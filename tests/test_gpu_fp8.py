@@ -71,7 +71,8 @@ def test_fp8_decode_matches_oracle(cuda, splits, window):
     assert_parity(out, ref, f"fp8 decode splits={splits} window={window}")
 
 
-@pytest.mark.parametrize("H,Hkv,D,bs", [(40, 8, 128, 16), (8, 8, 64, 32), (16, 2, 128, 8)])
+@pytest.mark.parametrize("H,Hkv,D,bs", [(40, 8, 128, 16), (8, 8, 64, 32), (16, 2, 128, 8),
+                                        (24, 2, 64, 16), (32, 2, 128, 16), (20, 1, 128, 16)])
 def test_fp8_decode_shapes(cuda, H, Hkv, D, bs):
     case, kc, vc, s = _fp8_case(cuda, H, Hkv, D, [5, 64, 333], bs=bs, seed=103, kv_scale=0.1)
     out = pa.pa_decode_fp8(case.q, torch.from_numpy(kc).to(cuda), torch.from_numpy(vc).to(cuda),

@@ -228,3 +228,20 @@ def test_mixed_call_orders_later_stream_work_after_the_prefill(cuda):
     assert pa.pa_read_device_error(device=cuda) == 0
     assert not torch.isnan(out).any()
     assert torch.equal(snap.view(torch.int16), out.view(torch.int16))
+
+
+def test_mixed_call_with_only_single_row_sequences(cuda):
+    # Every sequence has one query row although max_seqlen_q says 4: the prefill kernel
+    # has no item (one CTA, which exits) and the decode launch beside it does all rows.
+    w = Workload("dec_only", 32, 8, 128, 16, ())
+    case = make_case_from_lengths(w, [0, 15, 300, 2000], [1, 1, 1, 1], seed=55, device=cuda)
+    h = host_inputs(case)
+    oracle_store(case, h)
+    ref = oracle_attention(case, h)
+    m = device_tensors(case, cuda)
+    out = pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"],
+                               m["seq_lens"], m["block_table"], 4, case.max_seq_len,
+                               w.final_scale, 0, key=case.key, value=case.value,
+                               slot_mapping=m["slot_mapping"])
+    assert pa.pa_read_device_error(device=cuda) == 0
+    assert_parity(out, ref, "single-row sequences, max_seqlen_q = 4")
