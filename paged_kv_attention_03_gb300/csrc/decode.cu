@@ -43,6 +43,15 @@ namespace {
 // at head_dim 128) and at most 168 registers a thread, so three fit.  More resident CTAs
 // hide the pipeline fill at each CTA's start behind the other CTAs' streaming.
 constexpr int kDecodeCtasPerSm = 3;
+// The FP8 cache: a 3-stage ring of fp8 tiles (48 KB at head_dim 128); with one n-tile of
+// heads the kernel fits 128 registers, so four CTAs (16 warps) hide more latency.
+constexpr int kFp8Stages = 3;
+constexpr int kDecodeCtasPerSmFp8 = 4;
+
+template <bool FP8, int NT>
+constexpr int decode_ctas_per_sm() {
+    return FP8 && NT == 1 ? kDecodeCtasPerSmFp8 : kDecodeCtasPerSm;
+}
 
 using sm100::ex2_approx;
 
@@ -228,13 +237,12 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     constexpr int CPR = D / 8;                // 16-byte chunks per row
     constexpr int KSTEPS = D / 16;
     constexpr int DTILES = D / 8;
-    // FP8 ring: 16-key tiles of D bytes per row, twice as many stages in the same space.
+    // FP8 ring: 16-key tiles of D bytes per row.
     constexpr int TILE8 = 16 * D;
     constexpr int STAGE8 = 2 * TILE8;
     constexpr int CPR8 = D / 16;  // 16-byte chunks per fp8 row
-    constexpr int NST = FP8 ? 2 * NSTAGES : NSTAGES;  // ring depth
-    constexpr int SB = FP8 ? STAGE8 : STAGE_BYTES;     // bytes per stage
-    static_assert(NST * SB <= NSTAGES * STAGE_BYTES, "the ring fits the per-warp share");
+    constexpr int NST = FP8 ? kFp8Stages : NSTAGES;  // ring depth
+    constexpr int SB = FP8 ? STAGE8 : STAGE_BYTES;   // bytes per stage
 
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -385,7 +393,7 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     const int u_last = (hi - 1) >> 4;
     const int32_t *bt_row = p.block_table + static_cast<int64_t>(b) * p.max_num_blocks;
     const int bs_mask = (1 << p.log2_bs) - 1;
-    uint8_t *my_stages = smem + warp * NSTAGES * STAGE_BYTES;  // NST stages of SB bytes
+    uint8_t *my_stages = smem + warp * NST * SB;  // NST stages of SB bytes
     const uint32_t stage_base = smem_u32(my_stages);
     const uint64_t policy = l2_policy_evict_first();
 
@@ -562,7 +570,10 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
         // Scale, mask (edge units only), online softmax per head column: elements 0, 1 are
         // key u*16 + lane/4, elements 2, 3 key + 8; elements 0, 2 head 2t, 1, 3 head 2t+1.
         const bool edge = u * 16 < lo || u * 16 + 16 > hi;
-        float mx[NT][2];
+        // The reference maximum only moves when a score exceeds it by more than 8, so the
+        // column maxima (three dependent shuffles per head) are formed only when some
+        // score of the warp does; otherwise nothing changes.
+        bool over = false;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
@@ -573,33 +584,24 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
                     if (key < lo || key >= hi) v = -INFINITY;
                 }
                 s[j][e] = v;
+                over |= v > m_run[j][e & 1] + 8.f;
             }
-            mx[j][0] = fmaxf(s[j][0], s[j][2]);
-            mx[j][1] = fmaxf(s[j][1], s[j][3]);
         }
-        bool need = false;
-        float m_new[NT][2];
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float m = mx[j][e];
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                m_new[j][e] = fmaxf(m_run[j][e], m);
-                need |= m_new[j][e] > m_run[j][e] + 8.f;
-            }
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 float f[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool nd = m_new[j][e] > m_run[j][e] + 8.f;
-                    f[e] = nd ? ex2_approx(m_run[j][e] - m_new[j][e]) : 1.f;
+                    float m = fmaxf(s[j][e], s[j][e + 2]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    const float m_new = fmaxf(m_run[j][e], m);
+                    const bool nd = m_new > m_run[j][e] + 8.f;
+                    f[e] = nd ? ex2_approx(m_run[j][e] - m_new) : 1.f;
                     l_run[j][e] *= f[e];
-                    if (nd) m_run[j][e] = m_new[j][e];
+                    if (nd) m_run[j][e] = m_new;
                 }
 #pragma unroll
                 for (int mt = 0; mt < DTILES / 2; ++mt) {
@@ -748,7 +750,7 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
 }
 
 template <int D, int NWARPS, int NSTAGES, bool FP8, int NT>
-__global__ void __launch_bounds__(NWARPS * 32, kDecodeCtasPerSm) decode_split_kernel(const DecodeKernelParams p) {
+__global__ void __launch_bounds__(NWARPS * 32, (decode_ctas_per_sm<FP8, NT>())) decode_split_kernel(const DecodeKernelParams p) {
     decode_split_body<D, NWARPS, NSTAGES, FP8, NT>(p);
     // As a programmatic dependent of the prefill kernel of the same call (single-row
     // sequences of a varlen batch, or a cascade's suffix) the CTAs run beside the prefill
@@ -870,15 +872,15 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 2;
 
-template <int D>
+template <int D, bool FP8>
 constexpr int decode_smem_bytes() {
-    return kDecodeWarps * kDecodeStages * 2 * 16 * D * 2;
+    return FP8 ? kDecodeWarps * kFp8Stages * 2 * 16 * D : kDecodeWarps * kDecodeStages * 2 * 16 * D * 2;
 }
 
 template <int D, bool FP8>
 cudaError_t launch_decode_d(const DecodeKernelParams &kp, const DecodePlan &plan, int batch,
                             cudaStream_t stream) {
-    constexpr int smem = decode_smem_bytes<D>();
+    constexpr int smem = decode_smem_bytes<D, FP8>();
     static_assert(smem >= (kDecodeWarps * 16 * 2 + kDecodeWarps * 16 * (D + 4)) * 4,
                   "merge area must fit in the stage ring");
     // 8 heads per n-tile: a group of at most 8 query heads takes one, larger ones two.
