@@ -65,7 +65,7 @@ class L2Flush:
 # DRAM bytes (read + write) of one launch on the default workloads, from the ncu
 # captures summarised in profiles/ (commands there); None once a kernel changes.
 NCU_TRAFFIC = {
-    "decode_split_kernel": 639.53e6 + 4.34e6,
+    "decode_split_kernel": 639.53e6 + 3.92e6,
     "prefill_kernel": 313.81e6 + 104.57e6,
 }
 
