@@ -12,21 +12,25 @@
 //    share a kv head sit in the same CTA, so each K/V byte is read from HBM once per
 //    kv head, not once per query head.
 //  * The split's key range is cut into 16-key units; warp w takes units w, w + NW,
-//    ... and streams them through its own NSTAGES-deep cp.async ring (16-byte
-//    copies, XOR-swizzled so ldmatrix is bank-conflict free).  Block-table lookups
-//    are per key row, so any power-of-two block_size works.
-//  * S = Q K^T and O += P V run on the bf16 warp MMA (m16n8k16, fp32 accumulate)
-//    with the query heads of the group as the M = 16 rows.  Decode is HBM bound; the
-//    MMA only keeps the issue slots free (a CUDA-core dot product would need about
-//    one FFMA per loaded element per query head).
-//  * Online softmax in the base-2 domain with 2-step warp shuffles per row; the
-//    warps of a CTA merge their (m, l, O) through shared memory; a split writes
-//    either the final bf16 row (single split) or a normalised fp32 partial plus
-//    (m, l) to the workspace for decode_combine_kernel, which is launched with
-//    programmatic stream serialization so its launch overlaps the splits' tail.
+//    ... and streams them through its own cp.async ring (16-byte copies, XOR-swizzled
+//    so ldmatrix is bank-conflict free).  With block_size >= 16 a unit lies in one
+//    block: one table lookup and one 64-bit base per unit; smaller power-of-two blocks
+//    look up every key row.
+//  * S^T = K Q^T and O^T += V^T P^T run on the warp MMA (m16n8k16, fp32 accumulate)
+//    with the unit's 16 keys as the M rows and the query heads as N (8 per n-tile):
+//    with 4-5 query heads per kv head, heads as the M = 16 rows would leave 3/4 of each
+//    MMA and of the softmax as padding.  Decode is HBM bound; the MMA only keeps the
+//    issue slots free (a CUDA-core dot product would need about one FFMA per loaded
+//    element per query head).
+//  * Online softmax in the base-2 domain with a lazily moved reference maximum; the
+//    warps of a CTA merge their (m, l, O) through shared memory; a split writes either
+//    the final bf16 row (single split) or a normalised fp32 partial plus (m, l) to the
+//    workspace for decode_combine_kernel, which is launched with programmatic stream
+//    serialization so its launch overlaps the splits' tail.
 //  * Three CTAs per SM (2-stage rings, <= 168 registers) hide each other's pipeline
-//    fill; the FP8 instantiation keeps the codes fp8 in shared memory and runs f16
-//    MMAs on codes converted in registers.
+//    fill; the FP8 instantiation keeps the codes fp8 in shared memory (a 3-stage ring,
+//    four CTAs per SM with one head n-tile) and runs f16 MMAs on codes converted in
+//    registers.
 #include <math.h>
 
 #include <cuda_fp16.h>
