@@ -156,19 +156,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return h;
 }
 
-// acc += float(bf16 low half of v) + float(bf16 high half of v) (mixed-precision adds:
-// the bf16 halves go in directly, exactly).
-__device__ __forceinline__ void add_bf16x2_f32(float &acc, uint32_t v) {
-    asm("{\n"
-        ".reg .b16 l, h;\n"
-        "mov.b32 {l, h}, %1;\n"
-        "add.rn.f32.bf16 %0, l, %0;\n"
-        "add.rn.f32.bf16 %0, h, %0;\n"
-        "}\n"
-        : "+f"(acc)
-        : "r"(v));
-}
-
 // lo += float(f16 low half of v), hi += float(f16 high half of v) (mixed-precision adds).
 __device__ __forceinline__ void add_f16x2_f32(float &lo, float &hi, uint32_t v) {
     asm("{\n"
@@ -188,18 +175,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
     uint32_t d;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
-}
-
-// acc += float(f16 low half of v) + float(f16 high half of v) (mixed-precision adds).
-__device__ __forceinline__ void add_f16x2_f32(float &acc, uint32_t v) {
-    asm("{\n"
-        ".reg .b16 l, h;\n"
-        "mov.b32 {l, h}, %1;\n"
-        "add.rn.f32.f16 %0, l, %0;\n"
-        "add.rn.f32.f16 %0, h, %0;\n"
-        "}\n"
-        : "+f"(acc)
-        : "r"(v));
 }
 
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)

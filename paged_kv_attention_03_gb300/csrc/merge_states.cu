@@ -22,18 +22,6 @@ namespace pa {
 
 namespace {
 
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 template <int D>
 __global__ void __launch_bounds__(128) merge_states_kernel(MergeArgs a) {
     constexpr int PER_LANE = D / 32;
@@ -46,7 +34,7 @@ __global__ void __launch_bounds__(128) merge_states_kernel(MergeArgs a) {
         const int r = r0 + lane;
         if (r < R) M = fmaxf(M, a.lses[static_cast<int64_t>(r) * a.rows + row]);
     }
-    M = warp_max_f(M);
+    M = warp_max(M);
     float acc[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
@@ -77,7 +65,7 @@ __global__ void __launch_bounds__(128) merge_states_kernel(MergeArgs a) {
                 }
             }
         }
-        wsum = warp_sum_f(wsum);
+        wsum = warp_sum(wsum);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
