@@ -68,8 +68,8 @@ constexpr int NSV = 2;                   // V stages
 // MMA issuer.  The producer warpgroup gives up registers so that the
 // softmax threads, which hold a 128-column logit row, get 200.
 constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpSched = 11;
-constexpr uint32_t kRing = 8;   // item-info ring slots
-constexpr uint32_t kAhead = 7;  // items published beyond the last Q load (< kRing)
+constexpr uint32_t kRing = 16;  // item-info ring slots
+constexpr uint32_t kAhead = 14;  // items published beyond the last Q load (< kRing)
 constexpr int kThreads = 12 * 32;
 constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 96;
 static_assert(kRegsSoftmax * 256 + kRegsProducer * 128 <= 168 * kThreads,
