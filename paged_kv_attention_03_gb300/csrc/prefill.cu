@@ -29,9 +29,9 @@
 //  * One thread issues the MMAs in the order ... P0 V(t-1), S0(t), P1 V(t-1), S1(t) ...,
 //    so each softmax warpgroup works on its tile while the tensor core runs the other
 //    tile's products (ping-pong).
-//  * Warp roles: 0-3 and 4-7 are the two softmax warpgroups (200 registers each after
+//  * Warp roles: 0-3 and 4-7 are the two softmax warpgroups (208 registers each after
 //    setmaxnreg); 8 loads K, 9 issues MMAs, 10 loads V, 11 schedules the CTA's items and
-//    loads Q (96 registers).  A softmax thread owns one TMEM lane (accumulator row):
+//    loads Q (88 registers).  A softmax thread owns one TMEM lane (accumulator row):
 //    mask, online softmax in base 2 with the scale folded into the exponent, lazy O
 //    rescale (only when the running max grows by more than 2^8), epilogue.
 //  * The K and V producers issue one page box per lane, in parallel; an item's last K/V
@@ -66,12 +66,13 @@ constexpr int NSV = 2;                   // V stages
 // Warpgroups 0 and 1 (warps 0-3, 4-7) are the softmax of query tiles 0 and 1 (a warp
 // reaches the TMEM lanes 32 * (warp % 4) ...); warpgroup 2 holds the producers and the
 // MMA issuer.  The producer warpgroup gives up registers so that the
-// softmax threads, which hold a 128-column logit row, get 200.
+// softmax threads, which hold a 128-column logit row, get 208 (the launch's whole
+// 168 x 384 registers: 208 x 256 + 88 x 128).
 constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpSched = 11;
 constexpr uint32_t kRing = 16;  // item-info ring slots
 constexpr uint32_t kAhead = 14;  // items published beyond the last Q load (< kRing)
 constexpr int kThreads = 12 * 32;
-constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 96;
+constexpr uint32_t kRegsSoftmax = 208, kRegsProducer = 88;
 static_assert(kRegsSoftmax * 256 + kRegsProducer * 128 <= 168 * kThreads,
               "register split exceeds the launch's 168 per thread");
 constexpr uint32_t kTmemCols = 512;
