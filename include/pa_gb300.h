@@ -321,7 +321,9 @@ int pa_common_prefix_blocks(const int32_t *block_table, int batch, int max_num_b
  * [max(0, p - w + 1), p] (all keys <= p without a window).  sq_i == 1 rows are
  * legal, so a mixed prefill + decode batch may be passed as one call; when seq_lens is
  * given, those sequences run on the decode kernel within the call (no workspace needed)
- * while the tensor-core kernel takes the rest.
+ * while the tensor-core kernel takes the rest.  The decode kernel then runs at the same
+ * time, on the SMs the tensor-core kernel's items leave free; the call's work completes
+ * (in stream order) only after both kernels have finished.
  *
  *   out           [total_q, num_heads, head_dim] bf16, device (written)
  *   q             [total_q, num_heads, head_dim] bf16, device, 16-byte aligned
