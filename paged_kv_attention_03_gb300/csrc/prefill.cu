@@ -440,7 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rows1 = __reduce_add_sync(0xffffffffu, rows1);
                 const uint32_t v = pairs * static_cast<uint32_t>(Hkv);
                 if (rows1 != 0) {
-                    const uint32_t rounds = (v + P - 1) / P;
+                    // One round more when the decode rows outweigh the prefill items (with
+                    // K keys a row, decode time / prefill time ~ 0.68 rows1 / pairs).
+                    const uint32_t rounds = (v + P - 1) / P + (2u * rows1 >= 3u * pairs ? 1u : 0u);
                     P = v == 0 ? 1u : (v + rounds - 1) / rounds;
                 }
                 if (cta >= P) n_pairs = 0;
