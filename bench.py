@@ -66,7 +66,7 @@ class L2Flush:
 # captures summarised in profiles/ (commands there); None once a kernel changes.
 NCU_TRAFFIC = {
     "decode_split_kernel": 639.53e6 + 3.92e6,
-    "prefill_kernel": 315.92e6 + 104.46e6,
+    "prefill_kernel": 316.23e6 + 104.09e6,
 }
 
 
