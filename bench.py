@@ -63,10 +63,15 @@ class L2Flush:
                 f"the step; untimed)")
 
 # DRAM bytes (read + write) of one launch on the default workloads, from the ncu
-# captures summarised in profiles/ (commands there); None once a kernel changes.
+# captures summarised in the named profiles/ files (commands there), with the commit of
+# the kernel source they were taken on.  A changed kernel needs a new capture.
 NCU_TRAFFIC = {
-    "decode_split_kernel": 639.53e6 + 3.92e6,
-    "prefill_kernel": 316.23e6 + 104.09e6,
+    "decode_split_kernel": {"bytes": 639.53e6 + 3.92e6,
+                            "source": "profiles/decode_split_kernel_batched_decode.md",
+                            "kernel_commit": "4a9b103"},
+    "prefill_kernel": {"bytes": 316.23e6 + 104.09e6,
+                       "source": "profiles/prefill_kernel_varlen_prefill.md",
+                       "kernel_commit": "4a9b103"},
 }
 
 
@@ -336,6 +341,13 @@ class MixedRunner:
     def single(self):
         self.full.step()
 
+    def chunks_only(self):
+        w = self.case.workload
+        self.pa.pa_varlen_prefill(self.pq, self.case.k_cache, self.case.v_cache, self.pcu,
+                                  self.psl, self.pbt, self.pmax_q, self.pmax_k, w.final_scale,
+                                  w.sliding_window, key=self.pkey, value=self.pval,
+                                  slot_mapping=self.pslots, out=self.pout)
+
     def split(self):
         w = self.case.workload
         self.pa.pa_varlen_prefill(self.pq, self.case.k_cache, self.case.v_cache, self.pcu,
@@ -514,6 +526,8 @@ def main():
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-long", action="store_true")
+    ap.add_argument("--no-tiny", action="store_true")
     ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
                     help="decode: the decode step only; prefill: the prefill step only "
                          "(profiling runs); both: the full JSON line")
@@ -613,6 +627,13 @@ def main():
     if not args.no_fp8:
         fp8 = _fp8_leg(pa, dev, rank, peaks, flush, stream, args, case, runner)
 
+    long_dec = None
+    if not args.no_long and args.workload != "long_decode":
+        long_dec = _long_decode_leg(pa, dev, rank, peaks, flush, stream, args)
+    tiny = None
+    if not args.no_tiny and args.workload != "tiny_decode":
+        tiny = _tiny_decode_leg(pa, dev, rank, peaks, flush, stream, args)
+
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and args.gpus == 1:
         t_s, threads, reps = oracle_decode_time(case, runner.seqs)
@@ -637,9 +658,11 @@ def main():
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"],
-                     "traffic": (NCU_TRAFFIC["decode_split_kernel"]
+                     "traffic": (NCU_TRAFFIC["decode_split_kernel"]["bytes"]
                                  if args.workload == "batched_decode" else None),
                      "traffic_kernel": "decode_split_kernel",
+                     "traffic_source": (NCU_TRAFFIC["decode_split_kernel"]
+                                        if args.workload == "batched_decode" else None),
                      "algorithmic_bytes": runner.work,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
                      "achieved_after_write_only_flush": round(
@@ -657,6 +680,10 @@ def main():
         line["cascade"] = cascade
     if fp8 is not None:
         line["fp8_decode"] = fp8
+    if long_dec is not None:
+        line["long_decode"] = long_dec
+    if tiny is not None:
+        line["tiny_decode"] = tiny
     print(json.dumps(line), flush=True)
 
 
@@ -708,23 +735,91 @@ def _cascade_leg(pa, dev, rank, peaks, flush, stream, args):
 
 
 def _mixed_leg(pa, dev, rank, peaks, flush, stream, args):
-    """Step time of the mixed-window workload, one call and two calls, against the step's
-    roofline time: decode bytes / HBM peak + chunk FLOPs / bf16 peak."""
+    """The mixed-window workload (chunked prefill + decodes, window 4096): the one-call
+    step, the two-call step, and each part alone against its own roofline.  The step is
+    reported against two bounds: the serial sum (decode bytes / HBM peak + chunk FLOPs /
+    bf16 peak) and the overlapped max() of the two, which the one-call design aims at
+    because its decode CTAs run beside the prefill kernel."""
     case = make_case(WORKLOADS["mixed_window"], seed=200 + rank, device=dev)
     runner = MixedRunner(case, dev)
     steps = max(20, args.steps // 10)
     single = statistics.mean(_time_steps(runner.single, steps, 3, flush, stream))
     split = statistics.mean(_time_steps(runner.split, steps, 3, flush, stream))
-    roof_ms = 1e3 * (runner.decode_bytes / (peaks["hbm_gbs"] * 1e9) +
-                     runner.chunk_flops / (peaks["bf16_tflops"] * 1e12))
+    chunks = statistics.mean(_time_steps(runner.chunks_only, steps, 3, flush, stream))
+    decodes = statistics.mean(_time_steps(runner.dec.step, steps, 3, flush, stream))
+    dec_ms = 1e3 * runner.decode_bytes / (peaks["hbm_gbs"] * 1e9)
+    chunk_ms = 1e3 * runner.chunk_flops / (peaks["bf16_tflops"] * 1e12)
+    serial_ms, overlap_ms = dec_ms + chunk_ms, max(dec_ms, chunk_ms)
     return {"workload": f"mixed_window: {runner.n_chunks} chunks of 512 + "
                         f"{runner.n_decodes} decodes, ctx U[1024,8192], window 4096",
             "chunk_flops": runner.chunk_flops, "decode_bytes": runner.decode_bytes,
-            "roofline_ms": round(roof_ms, 4),
+            "roofline_ms": round(serial_ms, 4),
+            "roofline_ms_overlapped": round(overlap_ms, 4),
             "single_call": {"ms_per_step": round(single, 4), "launches": 3,
-                            "frac_of_roofline": round(roof_ms / single, 4)},
+                            "frac_of_roofline": round(serial_ms / single, 4),
+                            "frac_of_overlapped_bound": round(overlap_ms / single, 4)},
             "two_calls": {"ms_per_step": round(split, 4), "launches": 2 + runner.dec.launches,
-                          "frac_of_roofline": round(roof_ms / split, 4)}}
+                          "frac_of_roofline": round(serial_ms / split, 4),
+                          "frac_of_overlapped_bound": round(overlap_ms / split, 4)},
+            "chunks_alone": {"ms_per_step": round(chunks, 4),
+                             "tflops": round(runner.chunk_flops / (chunks / 1e3) / 1e12, 2),
+                             "frac_of_bf16_peak": round(chunk_ms / chunks, 4),
+                             "note": "store of the chunk tokens + prefill, one call"},
+            "decodes_alone": {"ms_per_step": round(decodes, 4),
+                              "gbs": round(runner.decode_bytes / (decodes / 1e3) / 1e9, 2),
+                              "frac_of_hbm": round(dec_ms / decodes, 4),
+                              "note": "pa_decode with the fused store, + combine"}}
+
+
+def _long_decode_leg(pa, dev, rank, peaks, flush, stream, args):
+    """Long-context decode (split-K stress): batch 8, 40/8 heads, seq_len U[32768, 131072];
+    store fused + split kernel + combine, with its own clock record."""
+    case = make_case(WORKLOADS["long_decode"], seed=rank, device=dev)
+    runner = DecodeRunner(case, dev)
+    steps = max(20, args.steps // 10)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(3):
+        flush()
+        runner.step()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    step = statistics.mean(_time_steps(runner.step, steps, 0, flush, stream))
+    attn = statistics.mean(_time_steps(runner.attention_only, steps, 3, flush, stream))
+    clocks = sampler.stop() if sampler else None
+    ach = runner.work / (attn / 1e3) / 1e9
+    del case
+    return {"workload": f"long_decode: {_describe(WORKLOADS['long_decode'])}, batch 8, "
+                        f"seq_len U[32768,131072]",
+            "kv_bytes_per_step": runner.work, "num_splits": runner.splits,
+            "ms_per_step": round(step, 4),
+            "gbs": round(runner.work / (step / 1e3) / 1e9, 2),
+            "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_split_kernel + combine)",
+                         "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(ach / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"]},
+            "clocks": clocks}
+
+
+def _tiny_decode_leg(pa, dev, rank, peaks, flush, stream, args):
+    """Tiny decode (4 sequences of {17, 33, 64, 100} keys, 8/2 heads, D=64): a latency
+    figure, microseconds per call, after an L2 flush (cold) and with the data left in L2
+    (warm).  Before each warm step a ~20 us spin kernel keeps the GPU busy while the host
+    queues the call, so the figure is device time, not host launch time."""
+    case = make_case(WORKLOADS["tiny_decode"], seed=0, device=dev)
+    runner = DecodeRunner(case, dev)
+    steps = max(50, args.steps // 5)
+    cold = statistics.median(_time_steps(runner.step, steps, 5, flush, stream))
+    warm = statistics.median(_time_steps(runner.step, steps, 5,
+                                         lambda: torch.cuda._sleep(40000), stream))
+    return {"workload": f"tiny_decode: {_describe(WORKLOADS['tiny_decode'])}, seq_lens "
+                        f"{{17,33,64,100}}",
+            "kv_bytes_per_step": runner.work,
+            "us_per_call_cold": round(cold * 1e3, 2), "us_per_call_warm": round(warm * 1e3, 2),
+            "launches": runner.launches,
+            "note": "median device time of one pa_decode call (store fused); the data fit "
+                    "in L2, so a roofline fraction is not meaningful"}
 
 
 def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):
@@ -749,7 +844,8 @@ def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):
                          "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
                          "peak_source": peaks["source"],
-                         "traffic": NCU_TRAFFIC["prefill_kernel"],
+                         "traffic": NCU_TRAFFIC["prefill_kernel"]["bytes"],
+                         "traffic_source": NCU_TRAFFIC["prefill_kernel"],
                          "algorithmic_flops": runner.work}}
 
 

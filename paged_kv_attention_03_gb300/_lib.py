@@ -7,6 +7,7 @@ so.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import functools
 import os
@@ -157,6 +158,46 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str, device: torch.device |
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _out(out: torch.Tensor | None, shape, dtype: torch.dtype, dev: torch.device,
+         name: str = "out") -> torch.Tensor:
+    """A caller-supplied output must match exactly (the kernels write shape's bytes);
+    None allocates one."""
+    if out is None:
+        return torch.empty(tuple(shape), dtype=dtype, device=dev)
+    _need(out, dtype, name, dev)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(out.shape)}")
+    if not out.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return out
+
+
+def _new_tokens(key, value, slot_mapping, rows: int, hkv: int, head_dim: int,
+                dev: torch.device, what: str) -> None:
+    """The optional store of new tokens: key/value [rows, Hkv, D] bf16 and slot_mapping
+    [rows] int32, all three or none."""
+    given = [t is not None for t in (key, value, slot_mapping)]
+    if not any(given):
+        return
+    if not all(given):
+        raise ValueError(f"{what}: key, value and slot_mapping are given together")
+    _need(key, torch.bfloat16, "key", dev)
+    _need(value, torch.bfloat16, "value", dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    if tuple(key.shape) != (rows, hkv, head_dim) or value.shape != key.shape:
+        raise ValueError(f"{what}: key/value must be [{rows}, {hkv}, {head_dim}]")
+    if tuple(slot_mapping.shape) != (rows,):
+        raise ValueError(f"{what}: slot_mapping must have {rows} entries")
+
+
+def _on(dev: torch.device):
+    """Make `dev` the current device for the call: the library takes the device of its
+    error word, scratch and shared-memory limits from the current device."""
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
+
+
 def pa_store_kvcache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
                      v_cache: torch.Tensor, slot_mapping: torch.Tensor) -> None:
     """Scatter key/value [T, Hkv, D] into k_cache/v_cache [NB, bs, Hkv, D] by slot_mapping [T]."""
@@ -170,8 +211,9 @@ def pa_store_kvcache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tens
         raise ValueError("store_kvcache: inconsistent shapes")
     if slot_mapping.shape[0] != key.shape[0]:
         raise ValueError("store_kvcache: slot_mapping length != number of tokens")
-    st = lib.pa_store_kvcache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
-                              _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d, _stream(dev))
+    with _on(dev):
+        st = lib.pa_store_kvcache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d, _stream(dev))
     _check(st, "pa_store_kvcache")
 
 
@@ -192,9 +234,10 @@ def pa_store_kvcache_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.
         raise ValueError("store_kvcache_fp8: inconsistent shapes")
     if slot_mapping.shape[0] != key.shape[0]:
         raise ValueError("store_kvcache_fp8: slot_mapping length != number of tokens")
-    st = lib.pa_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
-                                  _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d,
-                                  float(kv_scale), _stream(dev))
+    with _on(dev):
+        st = lib.pa_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(slot_mapping), key.shape[0], nb, bs, hkv, d,
+                                      float(kv_scale), _stream(dev))
     _check(st, "pa_store_kvcache_fp8")
 
 
@@ -217,19 +260,20 @@ def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     nb, bs, hkv, d = k_cache.shape
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
         raise ValueError("pa_decode_fp8: inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
+    _new_tokens(key, value, slot_mapping, batch, hkv, head_dim, dev, "pa_decode_fp8")
+    out = _out(out, q.shape, torch.bfloat16, dev)
     need = pa_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
                                     sliding_window, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = _ptr(workspace) if need else None
     ws_bytes = workspace.numel() * workspace.element_size() if need else 0
-    st = lib.pa_decode_fp8(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
-                           _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-                           _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
-                           head_dim, int(sliding_window), float(scale), float(kv_scale),
-                           int(num_splits), ws_ptr, ws_bytes, _stream(dev))
+    with _on(dev):
+        st = lib.pa_decode_fp8(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                               _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                               head_dim, int(sliding_window), float(scale), float(kv_scale),
+                               int(num_splits), ws_ptr, ws_bytes, _stream(dev))
     _check(st, "pa_decode_fp8")
     return out
 
@@ -266,19 +310,20 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     nb, bs, hkv, d = k_cache.shape
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
         raise ValueError("pa_decode: inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
+    _new_tokens(key, value, slot_mapping, batch, hkv, head_dim, dev, "pa_decode")
+    out = _out(out, q.shape, torch.bfloat16, dev)
     need = pa_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
                                     sliding_window, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = _ptr(workspace) if need else None
     ws_bytes = workspace.numel() * workspace.element_size() if need else 0
-    st = lib.pa_decode(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
-                       _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-                       _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
-                       head_dim, int(sliding_window), float(scale), int(num_splits), ws_ptr,
-                       ws_bytes, _stream(dev))
+    with _on(dev):
+        st = lib.pa_decode(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                           _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                           _ptr(seq_lens), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                           head_dim, int(sliding_window), float(scale), int(num_splits), ws_ptr,
+                           ws_bytes, _stream(dev))
     _check(st, "pa_decode")
     return out
 
@@ -311,21 +356,20 @@ def pa_decode_state(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     nb, bs, hkv, d = k_cache.shape
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
         raise ValueError("pa_decode_state: inconsistent shapes")
-    if state is None:
-        state = torch.empty(batch, num_heads, head_dim, dtype=torch.float32, device=dev)
-    if lse is None:
-        lse = torch.empty(batch, num_heads, dtype=torch.float32, device=dev)
+    state = _out(state, (batch, num_heads, head_dim), torch.float32, dev, "state")
+    lse = _out(lse, (batch, num_heads), torch.float32, dev, "lse")
     need = pa_decode_state_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
                                           sliding_window, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = _ptr(workspace) if need else None
     ws_bytes = workspace.numel() * workspace.element_size() if need else 0
-    st = lib.pa_decode_state(_ptr(state), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                             _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-                             _ptr(key_begin), batch, int(max_seq_len), nb, bs, num_heads, hkv,
-                             head_dim, int(sliding_window), float(scale), int(num_splits),
-                             ws_ptr, ws_bytes, _stream(dev))
+    with _on(dev):
+        st = lib.pa_decode_state(_ptr(state), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                 _ptr(key_begin), batch, int(max_seq_len), nb, bs, num_heads, hkv,
+                                 head_dim, int(sliding_window), float(scale), int(num_splits),
+                                 ws_ptr, ws_bytes, _stream(dev))
     _check(st, "pa_decode_state")
     return state, lse
 
@@ -344,10 +388,15 @@ def pa_merge_states(states: torch.Tensor, lses: torch.Tensor, out: torch.Tensor 
     rows = states[0].numel() // head_dim
     if lses.shape[0] != r or lses[0].numel() != rows:
         raise ValueError("pa_merge_states: states and lses disagree")
-    if out is None and want_bf16:
-        out = torch.empty(states.shape[1:], dtype=torch.bfloat16, device=dev)
-    st = lib.pa_merge_states(_ptr(out), _ptr(out_state), _ptr(out_lse), _ptr(states),
-                             _ptr(lses), r, rows, head_dim, _stream(dev))
+    if out is not None or want_bf16:
+        out = _out(out, states.shape[1:], torch.bfloat16, dev)
+    if out_state is not None:
+        _out(out_state, states.shape[1:], torch.float32, dev, "out_state")
+    if out_lse is not None:
+        _out(out_lse, lses.shape[1:], torch.float32, dev, "out_lse")
+    with _on(dev):
+        st = lib.pa_merge_states(_ptr(out), _ptr(out_state), _ptr(out_lse), _ptr(states),
+                                 _ptr(lses), r, rows, head_dim, _stream(dev))
     _check(st, "pa_merge_states")
     return out
 
@@ -391,17 +440,17 @@ def pa_cascade_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     nb, bs, hkv, d = k_cache.shape
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
         raise ValueError("pa_cascade_decode: inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, q.shape, torch.bfloat16, dev)
     need = pa_cascade_decode_workspace_size(batch, num_heads, hkv, head_dim, max_seq_len,
                                             prefix_len, sliding_window)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    st = lib.pa_cascade_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
-                               int(max_seq_len), int(prefix_len), nb, bs, num_heads, hkv,
-                               head_dim, int(sliding_window), float(scale), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(dev))
+    with _on(dev):
+        st = lib.pa_cascade_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+                                   int(max_seq_len), int(prefix_len), nb, bs, num_heads, hkv,
+                                   head_dim, int(sliding_window), float(scale), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(dev))
     _check(st, "pa_cascade_decode")
     return out
 
@@ -431,14 +480,15 @@ def pa_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     num_seqs = cu_seqlens_q.shape[0] - 1
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
         raise ValueError("pa_varlen_prefill: inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
-    st = lib.pa_varlen_prefill(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
-                               _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
-                               _ptr(cu_seqlens_k), _ptr(seq_lens), _ptr(block_table),
-                               block_table.shape[1], num_seqs, total_q, int(max_seqlen_q),
-                               int(max_seqlen_k), nb, bs, num_heads, hkv, head_dim,
-                               int(sliding_window), float(scale), _stream(dev))
+    _new_tokens(key, value, slot_mapping, total_q, hkv, head_dim, dev, "pa_varlen_prefill")
+    out = _out(out, q.shape, torch.bfloat16, dev)
+    with _on(dev):
+        st = lib.pa_varlen_prefill(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                   _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
+                                   _ptr(cu_seqlens_k), _ptr(seq_lens), _ptr(block_table),
+                                   block_table.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                                   int(max_seqlen_k), nb, bs, num_heads, hkv, head_dim,
+                                   int(sliding_window), float(scale), _stream(dev))
     _check(st, "pa_varlen_prefill")
     return out
 
@@ -483,11 +533,12 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     nb, bs, hkv, d = k_cache.shape
     if d != head_dim or block_table.dim() != 2 or block_table.shape[0] != batch:
         raise ValueError("pa_decode_noalloc: inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
-    st = fn(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
-            _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
-            int(max_seq_len), nb, bs, num_heads, hkv, head_dim, int(sliding_window),
-            float(scale), int(num_splits), _stream(dev))
+    _new_tokens(key, value, slot_mapping, batch, hkv, head_dim, dev, "pa_decode_noalloc")
+    out = _out(out, q.shape, torch.bfloat16, dev)
+    with _on(dev):
+        st = fn(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+                _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+                int(max_seq_len), nb, bs, num_heads, hkv, head_dim, int(sliding_window),
+                float(scale), int(num_splits), _stream(dev))
     _check(st, "pa_decode_noalloc")
     return out

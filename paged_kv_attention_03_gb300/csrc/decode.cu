@@ -106,6 +106,12 @@ struct DecodeKernelParams {
     // Varlen layout: sequence b is a decode row only if q_rows[b + 1] - q_rows[b] == 1;
     // its q / out row is q_rows[b] (null: row b).
     const int32_t *q_rows;
+    int total_q;        // rows of q / out in the varlen layout (q_rows bound)
+    // Varlen layout without a prefill launch in the same call: the split kernel checks
+    // the batch's query and key lengths itself (cu_k may be null).
+    int check_rows;
+    int max_seqlen_q;
+    const int32_t *cu_k;
     int after_prefill;  // launched as the prefill kernel's programmatic dependent
     unsigned *err;
 };
@@ -230,7 +236,19 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
     int qrow = b;  // q / out row of sequence b
     if (p.q_rows != nullptr) {
         const int r0 = p.q_rows[b];
-        if (p.q_rows[b + 1] - r0 != 1) return;  // not a single-row sequence
+        const int sq = p.q_rows[b + 1] - r0;
+        if (p.check_rows && split == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+            // No prefill kernel ran over this batch, so its length checks fall to here.
+            const int sk = p.seq_lens[b];
+            if (sq < 0 || sq > p.max_seqlen_q || sq > sk) flag_error(p.err, kErrQueryLen);
+            if (p.cu_k != nullptr && p.cu_k[b + 1] - p.cu_k[b] != sk)
+                flag_error(p.err, kErrSeqlensK);
+        }
+        if (sq != 1) return;  // not a single-row sequence
+        if (r0 < 0 || r0 >= p.total_q) {  // malformed cu_seqlens_q: no access out of bounds
+            if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(p.err, kErrQueryLen);
+            return;
+        }
         qrow = r0;
     }
     const int kvh = blockIdx.y / p.head_tiles;
@@ -933,14 +951,14 @@ bool plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int m
         // Enough CTAs for ~12 per SM over the run (4 per resident slot: load balance
         // across ragged lengths), but no split shorter than 256 keys (4 units per warp).
         const int64_t units = static_cast<int64_t>(batch) * num_kv_heads * p.head_tiles;
-        const int64_t target = 12LL * 152;
+        const int64_t target = 12LL * kPlanSms;
         int64_t s = (target + units - 1) / units;
         const int64_t by_len = (span + 255) / 256;
         if (s > by_len) s = by_len;
         // Long contexts: 8192-key chunks amortise each CTA's fixed cost (fill, merge)
         // better, as long as they still give two waves of resident CTAs.
         const int64_t s_long = (span + 8191) / 8192;
-        if (s_long >= 2 && s_long < s && units * s_long >= 2LL * kDecodeCtasPerSm * 152)
+        if (s_long >= 2 && s_long < s && units * s_long >= 2LL * kDecodeCtasPerSm * kPlanSms)
             s = s_long;
         splits = static_cast<int>(s);
     }
@@ -1009,6 +1027,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     kp.pre_lse = a.pre_lse;
     kp.pre_parts = a.pre_parts;
     kp.q_rows = a.q_rows;
+    kp.total_q = a.total_q;
+    kp.check_rows = a.check_rows ? 1 : 0;
+    kp.max_seqlen_q = a.max_seqlen_q;
+    kp.cu_k = a.cu_seqlens_k;
     kp.after_prefill = a.after_prefill ? 1 : 0;
     kp.err = a.err;
     if (a.fp8) {

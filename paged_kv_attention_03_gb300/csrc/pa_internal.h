@@ -30,6 +30,12 @@ cudaError_t launch_store_kvcache(const StoreArgs &a, cudaStream_t stream);
 cudaError_t launch_store_kvcache_fp8(const StoreArgs &a, float kv_scale, cudaStream_t stream);
 
 // ----------------------------------------------------------------- decode ---
+// SM count the decode split plan is made for.  The plan does not query the device, so
+// pa_decode_workspace_size stays a pure function of its arguments (callers size the
+// workspace before any device is chosen); it is also the fallback of sm_count() when
+// the device cannot be asked.
+constexpr int kPlanSms = 152;
+
 struct DecodePlan {
     int group;        // query heads per kv head
     int head_tiles;   // ceil(group / 16): 16-row MMA tiles per kv head
@@ -85,6 +91,12 @@ struct DecodeArgs {
     // Varlen layout (null: q / out rows are the sequences): sequence b is processed only
     // if q_rows[b + 1] - q_rows[b] == 1, with q / out row q_rows[b].
     const int32_t *q_rows;
+    int total_q;                   // number of q / out rows (bounds q_rows)
+    // With q_rows and no prefill launch over the batch: check every sequence's query
+    // length (0..max_seqlen_q, <= seq_lens) and cu_seqlens_k against seq_lens.
+    bool check_rows;
+    int max_seqlen_q;
+    const int32_t *cu_seqlens_k;   // may be null
     // Launch the split kernel as a programmatic dependent of the kernel before it (set
     // only right after the prefill kernel of the same call, which triggers its dependents
     // once all its CTAs are resident).  The split CTAs run beside the prefill; the grid's

@@ -92,6 +92,7 @@ struct PrefillKernelParams {
     const int32_t *block_table;
     int max_num_blocks;
     int num_seqs;
+    int total_q;  // rows of q / out
     int max_seqlen_q;
     int q_items;  // ceil(max_seqlen_q / (2 * tok_per_tile))
     int n_items;  // q_items * num_kv_heads * num_seqs
@@ -209,6 +210,11 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
     it.half_last = false;
     it.q_start = p.cu_q[it.seq];
     it.sq = p.cu_q[it.seq + 1] - it.q_start;
+    if (it.q_start < 0 || it.sq < 0 || static_cast<int64_t>(it.q_start) + it.sq > p.total_q) {
+        // Rows outside q / out (malformed cu_seqlens_q): flagged, never touched.
+        if (report) flag_error(p.err, kErrQueryLen);
+        return it;
+    }
     int sk;
     if (p.seq_lens != nullptr) {
         sk = p.seq_lens[it.seq];
@@ -1030,11 +1036,11 @@ bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uin
 int sm_count() {
     static std::atomic<int> counts[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kPlanSms;
     int n = counts[dev].load(std::memory_order_relaxed);
     if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
+            n = kPlanSms;
         counts[dev].store(n, std::memory_order_relaxed);
     }
     return n;
@@ -1078,6 +1084,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.block_table = a.block_table;
     kp.max_num_blocks = a.max_num_blocks;
     kp.num_seqs = a.num_seqs;
+    kp.total_q = a.total_q;
     kp.max_seqlen_q = a.max_seqlen_q;
     int log2_bs = 0;
     while ((1 << log2_bs) < a.block_size) ++log2_bs;
@@ -1134,6 +1141,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     d.sliding_window = a.sliding_window;
     d.scale = a.scale;
     d.q_rows = a.cu_seqlens_q;
+    d.total_q = a.total_q;
+    d.check_rows = !prefill_launched;
+    d.max_seqlen_q = a.max_seqlen_q;
+    d.cu_seqlens_k = a.cu_seqlens_k;
     d.after_prefill = prefill_launched;
     d.err = a.err;
     return launch_decode(d, plan, stream);

@@ -147,6 +147,15 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Copy a 128-row x 256-bit matrix from shared memory (matrix descriptor s_desc, the
+// operand layout an MMA reads) to tensor memory: row r -> lane r, its 32 bytes -> the 8
+// columns from taddr.  Asynchronous; it runs in issue order with this thread's later
+// tcgen05.mma, and a later tcgen05.commit tracks its completion.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc)
+                 : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -230,11 +239,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-}  // namespace sm100
-}  // namespace pa
-
-namespace pa {
-namespace sm100 {
 
 // Thread i of the warp writes 32 consecutive 32-bit columns of TMEM lane (taddr.lane + i).
 __device__ __forceinline__ void tmem_st_32x32b_x32_u(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -250,13 +254,7 @@ __device__ __forceinline__ void tmem_st_32x32b_x32_u(uint32_t taddr, const uint3
         : "memory");
 }
 
-}  // namespace sm100
-}  // namespace pa
 
-namespace pa {
-namespace sm100 {
-
-// Thread i of the warp writes 16 consecutive 32-bit columns of TMEM lane (taddr.lane + i).
 // tcgen05.wait::ld that names the destination registers of an earlier tcgen05.ld, so
 // the compiler cannot move a use of them above the wait.
 __device__ __forceinline__ void tmem_wait_ld_regs(float (&v)[32]) {
@@ -270,25 +268,6 @@ __device__ __forceinline__ void tmem_wait_ld_regs(float (&v)[32]) {
                  :
                  : "memory");
 }
-
-
-}  // namespace sm100
-}  // namespace pa
-
-namespace pa {
-namespace sm100 {
-
-
-
-
-
-
-
-}  // namespace sm100
-}  // namespace pa
-
-namespace pa {
-namespace sm100 {
 
 // ------------------------------------------------- programmatic dependent launch ---
 // Let the next kernel of the stream (launched with programmatic stream serialization)

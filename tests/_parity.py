@@ -64,24 +64,55 @@ def half_ulp(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return np.where(a > 0, np.exp2(e - _SIG_BITS[dtype]), 0.0)
 
 
+def round_to(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """fp64 values rounded once, to nearest even, to the significand of `dtype` (normal
+    range; the exponent range of the outputs here is far from its limits)."""
+    bits = _SIG_BITS[dtype]
+    m, e = np.frexp(ref)                       # ref = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, bits)), e - bits)  # rint: ties to even
+
+
+# Parity figures of the tests that ran, printed at the end of the session.
+RECORDS: list[tuple[str, dict]] = []
+
+
 def assert_parity(got: torch.Tensor, ref: np.ndarray, what: str = "",
                   max_abs: float = MAX_ABS, mean_abs: float = MEAN_ABS) -> dict:
-    """The stated bar is for the attention arithmetic (bf16 operands, fp32 accumulation);
-    the output's own rounding to its storage type (bf16 for attention rows) adds up to
-    half an ulp of the exact value, so element i may differ by max_abs + half_ulp(ref_i).
-    For |ref| < 1 that is at most 1e-2 + 2^-9; the mean-abs bar is unchanged."""
+    """Two bars, both asserted:
+
+    1. against the fp64 oracle: the stated bar is for the attention arithmetic (bf16
+       operands, fp32 accumulation); the output's own rounding to its storage type adds
+       up to half an ulp of the exact value, so element i may differ by
+       max_abs + half_ulp(ref_i) (for |ref| < 1 at most 1e-2 + 2^-9).
+    2. against the oracle rounded once to the output type: max-abs <= max_abs, except
+       where that type's spacing exceeds max_abs (|ref| >= 2 for bf16), where the output
+       must be the correctly rounded value or one of its two neighbours.
+    The mean-abs bar is against the fp64 oracle."""
     g = got.detach().float().cpu().double().numpy()
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - ref)
     excess = err - (max_abs + half_ulp(ref, got.dtype))
+    rr = round_to(ref, got.dtype)
+    err_r = np.abs(g - rr)
+    ulp = 2.0 * half_ulp(rr, got.dtype)
+    coarse = ulp > max_abs
     stats = {"max_abs": float(err.max()) if err.size else 0.0,
              "mean_abs": float(err.mean()) if err.size else 0.0,
-             "max_excess": float(excess.max()) if err.size else -max_abs}
+             "max_excess": float(excess.max()) if err.size else -max_abs,
+             "max_abs_vs_rounded": float(err_r[~coarse].max()) if (~coarse).any() else 0.0,
+             "coarse_elems": int(coarse.sum()),
+             "elems": int(err.size)}
+    RECORDS.append((what, stats))
     if err.size and stats["max_excess"] > 0:
         i = int(np.argmax(excess))
         raise AssertionError(f"{what}: |err| {err.flat[i]:.3e} at |ref| {abs(ref.flat[i]):.3f} "
                              f"exceeds {max_abs} + half an ulp ({half_ulp(ref.flat[i], got.dtype):.2e})")
+    assert stats["max_abs_vs_rounded"] <= max_abs, \
+        f"{what}: max-abs {stats['max_abs_vs_rounded']:.3e} against the rounded oracle > {max_abs}"
+    if coarse.any():
+        bad = err_r[coarse] > ulp[coarse] * 1.0000001
+        assert not bad.any(), f"{what}: an output with |ref| >= 2 is more than one ulp off"
     assert stats["mean_abs"] <= mean_abs, f"{what}: mean-abs {stats['mean_abs']:.3e} > {mean_abs}"
     return stats
 

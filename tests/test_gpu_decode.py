@@ -130,34 +130,43 @@ def test_decode_seq_len_beyond_declared_max_is_flagged(cuda):
     assert pa.pa_read_device_error(device=cuda) & pa.DEVERR_SEQ_RANGE
 
 
-def _sampled_check(case, dev, seqs, sample):
+def _whole_batch_check(case, dev, seqs, what):
+    """Store + decode of the decode sequences `seqs` in one launch configuration (the
+    benchmark's), every output row compared with the oracle."""
     h = host_inputs(case)
-    oracle_store(case, h)
+    rows = case.cu_seqlens_q[np.asarray(seqs)]  # the decode tokens only
+    oracle.store_kvcache(np.ascontiguousarray(h["key"][rows]),
+                         np.ascontiguousarray(h["value"][rows]), h["k_cache"], h["v_cache"],
+                         np.ascontiguousarray(case.slot_mapping[rows]), case.workload.block_size)
     out = _decode_case(case, dev, seqs=seqs)
     assert pa.pa_read_device_error(device=dev) == 0
-    pick = np.asarray(sample)
-    ref = oracle_attention(case, h, seqs=np.asarray(seqs)[pick])
-    return assert_parity(out[torch.as_tensor(pick, device=dev)], ref)
+    np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
+    ref = oracle_attention(case, h, seqs=np.asarray(seqs))
+    return assert_parity(out, ref, f"full size {what}")
 
 
 def test_decode_full_size_batched(cuda):
     # Batch 64, 32/8 heads, D=128, seq_len U[512, 4096], 32768-block pool: the launch
-    # configuration the benchmark times; 6 sequences (all heads) checked by the oracle.
+    # configuration the benchmark times; every sequence and head checked.
     case = make_case("batched_decode", seed=0, device=cuda)
-    order = np.argsort(case.seq_lens)
-    _sampled_check(case, cuda, np.arange(case.num_seqs),
-                   [order[0], order[1], order[31], order[-2], order[-1], 17])
+    _whole_batch_check(case, cuda, np.arange(case.num_seqs), "batched_decode")
 
 
 def test_decode_full_size_long_context(cuda):
     # Batch 8, 40/8 heads (group of 5), seq_len U[32768, 131072].
     case = make_case("long_decode", seed=0, device=cuda)
-    order = np.argsort(case.seq_lens)
-    _sampled_check(case, cuda, np.arange(case.num_seqs), [order[0], order[-1]])
+    _whole_batch_check(case, cuda, np.arange(case.num_seqs), "long_decode")
+
+
+def test_decode_full_size_tiny(cuda):
+    # 4 sequences of {17, 33, 64, 100} keys, 8/2 heads, D=64, scale 1/8.
+    case = make_case("tiny_decode", seed=0, device=cuda)
+    _whole_batch_check(case, cuda, np.arange(case.num_seqs), "tiny_decode")
 
 
 def test_decode_full_size_mixed_batch_decode_half(cuda):
     # The 128 decodes of the mixed workload, sliding window 4096.
     case = make_case("mixed_window", seed=0, device=cuda)
     _, dec = split_mixed(case)
-    _sampled_check(case, cuda, dec, [0, 5, 77, 127])
+    _whole_batch_check(case, cuda, dec, "mixed_window decodes (pa_decode)")

@@ -36,7 +36,7 @@ def _prefill(case, dev, window=None, fused_store=True, use_cu_k=False, both=Fals
                                 slot_mapping=slots, out=out)
 
 
-def _full_check(case, dev, window=None, **kw):
+def _full_check(case, dev, window=None, what=None, **kw):
     h = host_inputs(case)
     oracle_store(case, h)
     ref = oracle_attention(case, h, window=window)
@@ -45,7 +45,7 @@ def _full_check(case, dev, window=None, **kw):
     assert flags == 0, f"device error bits {flags:#x}"
     np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
     np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
-    return assert_parity(out, ref, case.workload.name)
+    return assert_parity(out, ref, what or case.workload.name)
 
 
 @pytest.mark.parametrize("name", ["varlen_prefill_small", "mixed_window_small"])
@@ -177,42 +177,18 @@ def test_prefill_stale_rows_past_the_sequence_are_ignored(cuda):
     assert_parity(out, ref)
 
 
-def _sampled_rows_check(case, dev, seqs, n_rows=24, seed=0):
-    """Run the whole-batch prefill (launch configuration of the benchmark) and compare
-    sampled rows of the given sequences with the oracle, row by row."""
-    w = case.workload
-    h = host_inputs(case)
-    oracle_store(case, h)
-    out = _prefill(case, dev)
-    flags = pa.pa_read_device_error(device=dev)
-    assert flags == 0, f"device error bits {flags:#x}"
-    rng = np.random.default_rng(seed)
-    got, ref = [], []
-    for i in seqs:
-        a, b = int(case.cu_seqlens_q[i]), int(case.cu_seqlens_q[i + 1])
-        sq, sk = b - a, int(case.seq_lens[i])
-        rows = sorted(set([0, sq - 1, min(sq - 1, 127), min(sq - 1, 128)] +
-                          list(rng.integers(0, sq, size=n_rows))))
-        for r in rows:
-            ref.append(oracle.attend_row(h["q"][a + r], h["k_cache"], h["v_cache"],
-                                         case.block_table[i], sk, sk - sq + r, w.num_heads,
-                                         w.num_kv_heads, w.sliding_window, w.final_scale))
-            got.append(out[a + r])
-    return assert_parity(torch.stack(got), np.stack(ref))
-
-
 def test_prefill_full_size_varlen(cuda):
-    # 16 prompts of U[128, 2048] tokens, 32/8 heads, D=128, bs=16: the benchmark's launch.
+    # 16 prompts of U[128, 2048] tokens, 32/8 heads, D=128, bs=16: the benchmark's launch
+    # (store + prefill in one call); every output row checked.
     case = make_case("varlen_prefill", seed=0, device=cuda)
-    order = np.argsort(case.query_lens)
-    _sampled_rows_check(case, cuda, [order[0], order[7], order[-1]])
+    _full_check(case, cuda, what="full size varlen_prefill")
 
 
 def test_prefill_full_size_mixed_chunks(cuda):
-    # 8 chunks of 512 over contexts U[1024, 8192] + 128 decodes, window 4096, in one call.
+    # 8 chunks of 512 over contexts U[1024, 8192] + 128 decodes, window 4096, in one call;
+    # every output row (chunk rows and decode rows) checked.
     case = make_case("mixed_window", seed=0, device=cuda)
-    pre, dec = split_mixed(case)
-    _sampled_rows_check(case, cuda, [pre[0], pre[3], pre[-1], dec[0], dec[-1]], n_rows=12)
+    _full_check(case, cuda, what="full size mixed_window (one pa_varlen_prefill call)")
 
 
 def test_mixed_call_orders_later_stream_work_after_the_prefill(cuda):
@@ -245,3 +221,40 @@ def test_mixed_call_with_only_single_row_sequences(cuda):
                                slot_mapping=m["slot_mapping"])
     assert pa.pa_read_device_error(device=cuda) == 0
     assert_parity(out, ref, "single-row sequences, max_seqlen_q = 4")
+
+
+def test_decode_only_batch_checks_its_lengths(cuda):
+    # max_seqlen_q = 1: no prefill kernel runs, so the decode launch of the call checks
+    # cu_seqlens_k against seq_lens itself.
+    w = Workload("dec_chk", 8, 2, 128, 16, ())
+    case = make_case_from_lengths(w, [10, 40, 7], [1, 1, 1], seed=56, device=cuda)
+    m = device_tensors(case, cuda)
+    cuk = np.zeros(case.num_seqs + 1, np.int32)
+    cuk[1:] = np.cumsum(case.seq_lens)
+    cuk[2:] += 1  # sequence 1 disagrees
+    pa.pa_read_device_error(clear=True, device=cuda)
+    out = pa.pa_varlen_prefill(case.q, case.k_cache, case.v_cache, m["cu_seqlens_q"],
+                               m["seq_lens"], m["block_table"], 1, case.max_seq_len,
+                               w.final_scale, 0, cu_seqlens_k=torch.as_tensor(cuk, device=cuda))
+    assert pa.pa_read_device_error(clear=True, device=cuda) & pa.DEVERR_SEQLENS_K
+    h = host_inputs(case)
+    assert_parity(out, oracle_attention(case, h), "decode-only batch, cu_seqlens_k flagged")
+
+
+@pytest.mark.parametrize("max_q", [1, 40])
+def test_rows_beyond_q_are_flagged_not_touched(cuda, max_q):
+    # cu_seqlens_q names rows past the end of q / out: those sequences are flagged and
+    # skipped (no row outside q / out is read or written), the others are computed.
+    w = Workload("rows", 8, 2, 128, 16, ())
+    lens = [1, 1, 1] if max_q == 1 else [40, 40, 40]
+    case = make_case_from_lengths(w, [20, 30, 50], lens, seed=57, device=cuda)
+    m = device_tensors(case, cuda)
+    rows = int(case.cu_seqlens_q[2])  # q and out hold only the first two sequences' rows
+    q = case.q[:rows].contiguous()
+    out = torch.full_like(q, float("nan"))
+    pa.pa_read_device_error(clear=True, device=cuda)
+    pa.pa_varlen_prefill(q, case.k_cache, case.v_cache, m["cu_seqlens_q"], m["seq_lens"],
+                         m["block_table"], max_q, case.max_seq_len, w.final_scale, 0, out=out)
+    assert pa.pa_read_device_error(clear=True, device=cuda) & pa.DEVERR_QUERY_LEN
+    h = host_inputs(case)
+    assert_parity(out, oracle_attention(case, h, seqs=[0, 1]), "rows within q")
