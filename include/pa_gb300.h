@@ -360,6 +360,21 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
  */
 pa_status pa_read_device_error(void *stream, uint32_t *flags, int clear);
 
+/*
+ * pa_debug_prefill_stall - testing aid for the device-side failure detection; the
+ * pages have no counterpart.  Every wait inside the prefill kernel (pa_varlen_prefill,
+ * the prefix part of pa_cascade_decode) gives up after a time limit, raises
+ * PA_DEVERR_TIMEOUT, lets the copies and products it issued land, frees its tensor
+ * memory and returns, so the context stays usable.
+ *   stall != 0: later prefill launches of this process hand out no work item, so the
+ *               first wait of every role runs out while nothing is in flight.
+ *   wait_limit_ns: the limit of every wait of later launches (0: the default 2 s).
+ * pa_debug_prefill_stall(0, 0) restores normal launches.  The setting is process-wide
+ * and read when a launch is made (not synchronised with launches on other threads).
+ * Returns PA_OK.
+ */
+pa_status pa_debug_prefill_stall(int stall, uint64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

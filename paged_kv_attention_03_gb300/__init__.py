@@ -36,6 +36,7 @@ from ._lib import (  # noqa: F401
     pa_decode_num_splits,
     pa_decode_workspace_size,
     pa_read_device_error,
+    pa_debug_prefill_stall,
     pa_store_kvcache,
     pa_varlen_prefill,
     status_string,

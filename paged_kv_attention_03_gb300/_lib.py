@@ -34,7 +34,7 @@ EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num
             "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string",
             "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states",
             "pa_cascade_decode_workspace_size", "pa_cascade_decode", "pa_common_prefix_blocks",
-            "pa_store_kvcache_fp8", "pa_decode_fp8")
+            "pa_store_kvcache_fp8", "pa_decode_fp8", "pa_debug_prefill_stall")
 
 
 class PAError(RuntimeError):
@@ -491,6 +491,16 @@ def pa_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                    int(sliding_window), float(scale), _stream(dev))
     _check(st, "pa_varlen_prefill")
     return out
+
+
+def pa_debug_prefill_stall(stall: bool, wait_limit_ns: int = 0) -> None:
+    """Testing aid: later prefill launches hand out no work item (stall) and every wait
+    gives up after wait_limit_ns (0: the default 2 s), raising DEVERR_TIMEOUT."""
+    lib = load()
+    fn = lib.pa_debug_prefill_stall
+    fn.argtypes = [ctypes.c_int, ctypes.c_uint64]
+    fn.restype = ctypes.c_int
+    _check(fn(1 if stall else 0, int(wait_limit_ns)), "pa_debug_prefill_stall")
 
 
 def pa_read_device_error(clear: bool = True, device: torch.device | None = None) -> int:

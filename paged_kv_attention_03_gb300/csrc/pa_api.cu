@@ -531,6 +531,11 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
     return from_cuda(pa::launch_prefill(a, s));
 }
 
+pa_status pa_debug_prefill_stall(int stall, uint64_t wait_limit_ns) {
+    pa::debug_prefill_stall(stall, wait_limit_ns);
+    return PA_OK;
+}
+
 pa_status pa_read_device_error(void *stream, uint32_t *flags, int clear) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);

@@ -131,6 +131,8 @@ struct PrefillArgs {
     unsigned *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+// Testing aid behind pa_debug_prefill_stall (process-wide; read at each prefill launch).
+void debug_prefill_stall(int stall, uint64_t wait_ns);
 
 // Shared-prefix (cascade) partial states: every request's decode query against the
 // prefix_len keys in the first prefix_len / block_size entries of block_table, split

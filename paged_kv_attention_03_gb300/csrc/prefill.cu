@@ -79,7 +79,7 @@ constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: S_i at 128 * i, O_i at 256 + 128 * i.
 __host__ __device__ constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
 __host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * static_cast<uint32_t>(i); }
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait (default)
 
 struct PrefillKernelParams {
     CUtensorMap tmap_q;
@@ -117,6 +117,8 @@ struct PrefillKernelParams {
     int chunk_tiles;
     // Sequences with one query row are left to the decode kernel of the same call.
     int skip_decode_rows;
+    uint64_t wait_ns;  // limit of every wait (kTimeoutNs unless a test lowers it)
+    int stall;         // testing aid: publish no work item, so every wait runs out
     unsigned *err;
 };
 
@@ -251,7 +253,7 @@ __device__ __forceinline__ Item get_item(const PrefillKernelParams &p, int idx, 
 
 // Bounded wait by one thread.
 __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      unsigned *err) {
+                                      unsigned *err, uint64_t limit_ns) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -259,7 +261,7 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile in
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) t0 = now;
-            if (now - t0 > kTimeoutNs) {
+            if (now - t0 > limit_ns) {
                 *abort_flag = 1;
                 flag_error(err, kErrTimeout);
                 return false;
@@ -270,7 +272,8 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile in
 
 // Bounded wait by a whole warp; every lane returns the same answer.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
-                                          volatile int *abort_flag, unsigned *err) {
+                                          volatile int *abort_flag, unsigned *err,
+                                          uint64_t limit_ns) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         const bool ok = mbar_try_wait(bar, parity);
@@ -279,7 +282,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
             bool stop = *abort_flag != 0;
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) t0 = now;
-            stop = stop || (now - t0 > kTimeoutNs);
+            stop = stop || (now - t0 > limit_ns);
             if (__any_sync(0xffffffffu, stop)) {
                 if ((threadIdx.x & 31) == 0) {
                     *abort_flag = 1;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_dec<kRegsProducer>();
         // Take ring slot ic (every consumer): false at the end of the list or on abort.
         auto take_item = [&](uint32_t ic, Item &it) -> bool {
-            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err))
+            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err, p.wait_ns))
                 return false;
             it = info[ic % kRing].it;
             const bool end = info[ic % kRing].end != 0;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t P = gridDim.x;
             const uint32_t cta = blockIdx.x;
             const int Hkv = p.num_kv_heads;
-            int n_pairs = p.n_items / Hkv;  // (query block, sequence) pairs
+            int n_pairs = p.stall ? 0 : p.n_items / Hkv;  // (query block, sequence) pairs
             if (!PREFIX && p.skip_decode_rows) {
                 // A batch whose single-row sequences go to the decode launch of the same
                 // call deals its items to only as many CTAs as the same number of rounds
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         const Item it = get_item<PREFIX>(p, idx, false);
                         if (pub >= kRing && !wait1(bar(B_IEMPTY + pub % kRing),
-                                                   ((pub / kRing) - 1) & 1, abort_flag, p.err)) {
+                                                   ((pub / kRing) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
                             ok = false;
                         } else {
                             info[pub % kRing].it = it;
@@ -553,14 +556,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (loaded == pub) break;  // the list is exhausted and every Q loaded
                 // Only a Q load can make progress: wait for its buffer.
-                if (lane == 0) ok = wait1(bar(B_QEMPTY), (loaded - 1) & 1, abort_flag, p.err);
+                if (lane == 0) ok = wait1(bar(B_QEMPTY), (loaded - 1) & 1, abort_flag, p.err, p.wait_ns);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
             }
-            // End of the list.
-            if (ok && lane == 0 && !*abort_flag &&
+            // End of the list (never marked under the stall testing aid: every other role's
+            // first wait then runs out, with nothing in flight).
+            if (ok && lane == 0 && !*abort_flag && !p.stall &&
                 (pub < kRing ||
-                 wait1(bar(B_IEMPTY + pub % kRing), ((pub / kRing) - 1) & 1, abort_flag, p.err))) {
+                 wait1(bar(B_IEMPTY + pub % kRing), ((pub / kRing) - 1) & 1, abort_flag, p.err, p.wait_ns))) {
                 info[pub % kRing].end = 1;
                 mbar_arrive(bar(B_IFULL + pub % kRing));
             }
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSK;
                     if (t >= NSK &&
-                        !wait_warp(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err)) {
+                        !wait_warp(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < it.n_tiles; ++j, ++t) {
                     const int st = t % NSV;
                     if (t >= NSV &&
-                        !wait_warp(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err)) {
+                        !wait_warp(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -623,8 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t prev_g = 0;
                 auto issue_pv = [&](int i, uint32_t gv, bool first, bool half) -> bool {
                     const uint32_t c = cnt[i]++;
-                    if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err)) return false;
-                    if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err))
+                    if (!wait1(bar(B_PFULL + i), c & 1, abort_flag, p.err, p.wait_ns)) return false;
+                    if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err, p.wait_ns))
                         return false;
                     tc_fence_after();
                     const uint32_t vbase = sV + (gv % NSV) * L::TILE;
@@ -660,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 for (;; ++ic) {
-                    if (!wait1(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err)) {
+                    if (!wait1(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -670,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (end) break;
                     // Finish the previous item before waiting for this item's Q, so its
                     // epilogue never waits on a Q load.
-                    if (!flush() || !wait1(bar(B_QFULL), ic & 1, abort_flag, p.err)) {
+                    if (!flush() || !wait1(bar(B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -683,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        if (!wait1(bar(B_KFULL + st), (g / NSK) & 1, abort_flag, p.err)) {
+                        if (!wait1(bar(B_KFULL + st), (g / NSK) & 1, abort_flag, p.err, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t c = 0;    // tiles this warpgroup has processed
         bool ok = true;
         for (uint32_t ic = 0; ok; ++ic) {
-            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err)) break;
+            if (!wait_warp(bar(B_IFULL + ic % kRing), (ic / kRing) & 1, abort_flag, p.err, p.wait_ns)) break;
             const Item it = info[ic % kRing].it;
             const bool end = info[ic % kRing].end != 0;
             __syncwarp();
@@ -752,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY;  // reference max (base-2 units) the weights use
             float l_sum = 0.f;
             for (int j = 0; j < it.n_tiles; ++j, ++gt, ++c) {
-                if (!wait_warp(bar(B_SFULL + wg), c & 1, abort_flag, p.err)) {
+                if (!wait_warp(bar(B_SFULL + wg), c & 1, abort_flag, p.err, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -848,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // either P V of this tile is issued) so 0 * V stays 0.
                 if (wg == 0 && ((it.sk - 1) / BN) == it.kt0 + j && (it.sk & 15) != 0) {
                     const int st = gt % NSV;
-                    if (!wait_warp(bar(B_VFULL + st), (gt / NSV) & 1, abort_flag, p.err)) {
+                    if (!wait_warp(bar(B_VFULL + st), (gt / NSV) & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -870,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16 rows (P V of the item's last tile is number c-1) ----
-            if (!wait_warp(bar(B_ODONE + wg), (c - 1) & 1, abort_flag, p.err)) {
+            if (!wait_warp(bar(B_ODONE + wg), (c - 1) & 1, abort_flag, p.err, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -1003,6 +1007,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side ---
 
+// Testing aid (pa_debug_prefill_stall): later launches publish no item / use this limit.
+std::atomic<int> g_debug_stall{0};
+std::atomic<uint64_t> g_debug_wait_ns{0};
+
+void set_launch_limits(PrefillKernelParams &kp) {
+    const uint64_t w = g_debug_wait_ns.load(std::memory_order_relaxed);
+    kp.wait_ns = w != 0 ? w : kTimeoutNs;
+    kp.stall = g_debug_stall.load(std::memory_order_relaxed);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1071,6 +1085,11 @@ cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cuda
 
 }  // namespace
 
+void debug_prefill_stall(int stall, uint64_t wait_ns) {
+    g_debug_wait_ns.store(wait_ns, std::memory_order_relaxed);
+    g_debug_stall.store(stall != 0 ? 1 : 0, std::memory_order_relaxed);
+}
+
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return cudaSuccess;
     const int64_t slots = a.num_blocks * a.block_size;
@@ -1104,6 +1123,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     kp.window = a.sliding_window;
     kp.scale_log2 = a.scale * kLog2e;
     kp.err = a.err;
+    set_launch_limits(kp);
     // Sequences with a single query row (decode rows of a mixed batch) would fill one
     // token of a 128-row tile: with seq_lens given, a single-split decode launch takes
     // them (it needs no workspace) and the prefill kernel skips them.
@@ -1198,6 +1218,7 @@ cudaError_t launch_prefix_states(const PrefixArgs &a, cudaStream_t stream) {
     kp.prefix_len = a.prefix_len;
     kp.chunk_tiles = a.chunk_tiles;
     kp.err = a.err;
+    set_launch_limits(kp);
     // The launcher's view of the call: requests as the tokens of one sequence.
     PrefillArgs pa_{};
     pa_.q = a.q;
