@@ -146,8 +146,10 @@ struct Layout {
     static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
+    // 16-byte aligned: the item-info slots after it are read as 16-byte vectors.
+    static constexpr uint32_t OFF_MISC = (OFF_BAR + NBARS * 8 + 15u) & ~15u;
     static constexpr uint32_t OFF_INFO = OFF_MISC + 16;   // item-info ring, kRing x 64 bytes
+    static_assert(OFF_INFO % 16 == 0, "item-info slots are read as 16-byte vectors");
     static constexpr uint32_t BYTES = OFF_INFO + kRing * 64;
     // At least 116 KB so a single CTA owns an SM (and all of its TMEM).
     static constexpr uint32_t SMEM = (BYTES + 1024 > 118784u ? BYTES + 1024 : 118784u);
@@ -294,6 +296,148 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------------------------ scheduler ---
+// Run by one whole warp per CTA.  The work list is ordered longest first.  Its valid items
+// (those with query rows) are dealt to the P CTAs in snake order: rank v goes to CTA v mod P
+// in even rounds and to CTA P - 1 - (v mod P) in odd ones, which evens out the CTAs' total
+// work.  The warp scans 32 list positions per step; every CTA scans the whole list, and
+// position i reports its input errors only in CTA i mod P (and only where `reporter`).
+// Items are published to the CTA's item ring up to kAhead beyond the last Q load, so the K
+// and V producers can run ahead across short items.  Q loads go through the callbacks:
+// q_free(l) (non-blocking) / q_wait(l) (bounded) tell whether the buffer of load l is free,
+// q_load(l, item, next item or null) issues it.
+template <bool PREFIX, class QFree, class QWait, class QLoad>
+__device__ __forceinline__ void schedule_items(const PrefillKernelParams &p, ItemSlot *info,
+                                               uint32_t bar_ifull, uint32_t bar_iempty,
+                                               volatile int *abort_flag, uint32_t P,
+                                               const uint32_t cta, const bool reporter,
+                                               QFree q_free, QWait q_wait, QLoad q_load) {
+    const int lane = threadIdx.x & 31;
+    const int T = p.tok_per_tile;
+    const int Hkv = p.num_kv_heads;
+    auto ifull = [&](uint32_t i) { return bar_ifull + 8u * i; };
+    auto iempty = [&](uint32_t i) { return bar_iempty + 8u * i; };
+    int n_pairs = p.stall ? 0 : p.n_items / Hkv;  // (query block, sequence) pairs
+    if (!PREFIX && p.skip_decode_rows) {
+        // A batch whose single-row sequences go to the decode launch of the same call deals
+        // its items to only as many CTAs as the same number of rounds needs; the decode
+        // launch (a programmatic dependent of this kernel) takes the SMs of the others,
+        // which find no item and exit.  Every CTA counts the same sequences, so all agree
+        // on P.
+        uint32_t pairs = 0, rows1 = 0;
+        for (int i = lane; i < p.num_seqs; i += 32) {
+            const int sq = p.cu_q[i + 1] - p.cu_q[i];
+            if (sq == 1)
+                ++rows1;
+            else if (sq > 1)
+                pairs += static_cast<uint32_t>(min((sq + 2 * T - 1) / (2 * T), p.q_items));
+        }
+        pairs = __reduce_add_sync(0xffffffffu, pairs);
+        rows1 = __reduce_add_sync(0xffffffffu, rows1);
+        const uint32_t v = pairs * static_cast<uint32_t>(Hkv);
+        if (rows1 != 0) {
+            // One round more when the decode rows outweigh the prefill items (with K keys a
+            // row, decode time / prefill time ~ 0.68 rows1 / pairs).
+            const uint32_t rounds = (v + P - 1) / P + (2u * rows1 >= 3u * pairs ? 1u : 0u);
+            P = v == 0 ? 1u : (v + rounds - 1) / rounds;
+        }
+        if (cta >= P) n_pairs = 0;
+    }
+    // Target slot of round r: the snake order.
+    auto target = [&](uint32_t r) -> uint32_t { return r * P + ((r & 1u) ? P - 1u - cta : cta); };
+    uint32_t pub = 0, loaded = 0;  // items published / whose Q is loaded
+    uint32_t vrank = 0;            // valid items in the scanned part of the list
+    int scan = 0, win = 0;         // next pair to scan; first pair of the window
+    uint32_t mine = 0;             // window pairs holding items of this CTA
+    uint32_t r0_lane = 0;          // this lane's pair: rank of its first item
+    int cur = -1;                  // pair being enumerated (window lane), or -1
+    uint32_t cur_r0 = 0, cur_round = 0;
+    bool ok = true;
+    // One step per iteration, so a Q load (which gates the item's first S product) never
+    // waits behind a scan: load Q when its buffer is free, else scan one window or publish
+    // one item, else wait for the Q buffer.
+    for (;;) {
+        if (loaded < pub) {
+            bool ready = true;
+            if (lane == 0) ready = q_free(loaded);
+            if (__shfl_sync(0xffffffffu, ready, 0)) {
+                // The slots are intact: pub <= loaded + kAhead < loaded + kRing.
+                if (lane == 0)
+                    q_load(loaded, info[loaded % kRing].it,
+                           loaded + 1 < pub ? &info[(loaded + 1) % kRing].it : nullptr);
+                ++loaded;
+                continue;
+            }
+        }
+        if (pub < loaded + kAhead && (cur >= 0 || mine != 0 || scan < n_pairs)) {
+            if (cur < 0 && mine == 0) {
+                // Scan 32 pairs: the kv heads of a pair are all valid or none.
+                const int pp = scan + lane;
+                const bool v = pp < n_pairs &&
+                               get_item<PREFIX>(p, pp * Hkv,
+                                                reporter && static_cast<uint32_t>(pp) % P == cta)
+                                   .valid;
+                const uint32_t vm = __ballot_sync(0xffffffffu, v);
+                r0_lane = vrank + static_cast<uint32_t>(Hkv) * __popc(vm & ((1u << lane) - 1u));
+                // Does one of this CTA's ranks fall in [r0, r0 + Hkv)?  Only the first two
+                // rounds from r0 / P can hold the first one.
+                bool own = false;
+                if (v) {
+                    const uint32_t r = r0_lane / P;
+                    const uint32_t t0 = target(r), t1 = target(r + 1);
+                    own = (t0 >= r0_lane && t0 < r0_lane + Hkv) || t1 < r0_lane + Hkv;
+                }
+                mine = __ballot_sync(0xffffffffu, own);
+                win = scan;
+                scan += 32;
+                vrank += static_cast<uint32_t>(Hkv) * __popc(vm);
+                continue;
+            }
+            if (cur < 0) {
+                cur = __ffs(mine) - 1;
+                mine &= mine - 1u;
+                cur_r0 = __shfl_sync(0xffffffffu, r0_lane, cur);
+                cur_round = cur_r0 / P;
+            }
+            const uint32_t tv = target(cur_round++);
+            if (tv < cur_r0) continue;
+            if (tv >= cur_r0 + Hkv) {
+                cur = -1;
+                continue;
+            }
+            const int idx = (win + cur) * Hkv + static_cast<int>(tv - cur_r0);
+            if (lane == 0) {
+                const Item it = get_item<PREFIX>(p, idx, false);
+                if (pub >= kRing && !wait1(iempty(pub % kRing), ((pub / kRing) - 1) & 1,
+                                           abort_flag, p.err, p.wait_ns)) {
+                    ok = false;
+                } else {
+                    info[pub % kRing].it = it;
+                    info[pub % kRing].end = 0;
+                    mbar_arrive(ifull(pub % kRing));
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++pub;
+            continue;
+        }
+        if (loaded == pub) break;  // the list is exhausted and every Q loaded
+        // Only a Q load can make progress: wait for its buffer.
+        if (lane == 0) ok = q_wait(loaded);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+    }
+    // End of the list (never marked under the stall testing aid: every other role's first
+    // wait then runs out, with nothing in flight).
+    if (ok && lane == 0 && !*abort_flag && !p.stall &&
+        (pub < kRing || wait1(iempty(pub % kRing), ((pub / kRing) - 1) & 1, abort_flag, p.err,
+                              p.wait_ns))) {
+        info[pub % kRing].end = 1;
+        mbar_arrive(ifull(pub % kRing));
+    }
+}
+
 // 32-byte global store (the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *w) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
@@ -419,155 +563,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (warp == kWarpSched) {
             // ---------------- scheduler + Q producer (whole warp) ----------------
-            // The work list is ordered longest first.  Its valid items (those with query
-            // rows) are dealt to the CTAs in snake order: rank v goes to CTA v mod P in
-            // even rounds and to CTA P - 1 - (v mod P) in odd ones, which evens out the
-            // CTAs' total work.  The warp scans 32 list positions per step; every CTA
-            // scans the whole list, and position i reports its input errors only in CTA
-            // i mod P.  Items are published up to kAhead beyond the last Q load, so the K
-            // and V producers can run ahead across short items.
             if (lane == 0) prefetch_tmap(&p.tmap_q);
-            uint32_t P = gridDim.x;
-            const uint32_t cta = blockIdx.x;
-            const int Hkv = p.num_kv_heads;
-            int n_pairs = p.stall ? 0 : p.n_items / Hkv;  // (query block, sequence) pairs
-            if (!PREFIX && p.skip_decode_rows) {
-                // A batch whose single-row sequences go to the decode launch of the same
-                // call deals its items to only as many CTAs as the same number of rounds
-                // needs; the decode launch (a programmatic dependent of this kernel) takes
-                // the SMs of the others, which find no item and exit.  Every CTA counts the
-                // same sequences, so all agree on P.
-                uint32_t pairs = 0, rows1 = 0;
-                for (int i = lane; i < p.num_seqs; i += 32) {
-                    const int sq = p.cu_q[i + 1] - p.cu_q[i];
-                    if (sq == 1)
-                        ++rows1;
-                    else if (sq > 1)
-                        pairs += static_cast<uint32_t>(min((sq + 2 * T - 1) / (2 * T), p.q_items));
-                }
-                pairs = __reduce_add_sync(0xffffffffu, pairs);
-                rows1 = __reduce_add_sync(0xffffffffu, rows1);
-                const uint32_t v = pairs * static_cast<uint32_t>(Hkv);
-                if (rows1 != 0) {
-                    // One round more when the decode rows outweigh the prefill items (with
-                    // K keys a row, decode time / prefill time ~ 0.68 rows1 / pairs).
-                    const uint32_t rounds = (v + P - 1) / P + (2u * rows1 >= 3u * pairs ? 1u : 0u);
-                    P = v == 0 ? 1u : (v + rounds - 1) / rounds;
-                }
-                if (cta >= P) n_pairs = 0;
-            }
-            // Target slot of round r: the snake order.
-            auto target = [&](uint32_t r) -> uint32_t { return r * P + ((r & 1u) ? P - 1u - cta : cta); };
-            uint32_t pub = 0, loaded = 0;  // items published / whose Q is loaded
-            uint32_t vrank = 0;            // valid items in the scanned part of the list
-            int scan = 0, win = 0;         // next pair to scan; first pair of the window
-            uint32_t mine = 0;             // window pairs holding items of this CTA
-            uint32_t r0_lane = 0;          // this lane's pair: rank of its first item
-            int cur = -1;                  // pair being enumerated (window lane), or -1
-            uint32_t cur_r0 = 0, cur_round = 0;
-            bool ok = true;
-            // One step per iteration, so a Q load (which gates the item's first S product)
-            // never waits behind a scan: load Q when its buffer is free, else scan one
-            // window or publish one item, else wait for the Q buffer.
-            for (;;) {
-                if (loaded < pub) {
-                    bool ready = true;
-                    if (lane == 0 && loaded >= 1) ready = mbar_test_wait(bar(B_QEMPTY), (loaded - 1) & 1);
-                    if (__shfl_sync(0xffffffffu, ready, 0)) {
-                        if (lane == 0) {
-                            // The slot is intact: pub <= loaded + kAhead < loaded + kRing.
-                            const Item it = info[loaded % kRing].it;
-                            mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
+            // Q0 and Q1 of an item share one buffer pair, free once the previous item's last
+            // S products have read it.
+            auto q_free = [&](uint32_t l) -> bool {
+                return l == 0 || mbar_test_wait(bar(B_QEMPTY), (l - 1) & 1);
+            };
+            auto q_wait = [&](uint32_t l) -> bool {
+                return wait1(bar(B_QEMPTY), (l - 1) & 1, abort_flag, p.err, p.wait_ns);
+            };
+            auto q_load = [&](uint32_t, const Item &it, const Item *nit) {
+                mbar_arrive_expect_tx(bar(B_QFULL), q_tile_bytes * (it.has1 ? 2u : 1u));
 #pragma unroll
-                            for (int h = 0; h < NHALF; ++h) {
-                                tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
-                                            it.q_start + it.q0, bar(B_QFULL));
-                                if (it.has1)
-                                    tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64,
-                                                it.kvh * G, it.q_start + it.q0 + T, bar(B_QFULL));
-                            }
-                            if (loaded + 1 < pub) {  // pull the next item's Q into L2
-                                const Item nit = info[(loaded + 1) % kRing].it;
+                for (int h = 0; h < NHALF; ++h) {
+                    tma_load_3d(sQ + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                it.q_start + it.q0, bar(B_QFULL));
+                    if (it.has1)
+                        tma_load_3d(sQ + L::TILE + h * HALF, &p.tmap_q, h * 64, it.kvh * G,
+                                    it.q_start + it.q0 + T, bar(B_QFULL));
+                }
+                if (nit != nullptr) {  // pull the next item's Q into L2
 #pragma unroll
-                                for (int h = 0; h < NHALF; ++h) {
-                                    tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
-                                                       nit.q_start + nit.q0);
-                                    if (nit.has1)
-                                        tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit.kvh * G,
-                                                           nit.q_start + nit.q0 + T);
-                                }
-                            }
-                        }
-                        ++loaded;
-                        continue;
+                    for (int h = 0; h < NHALF; ++h) {
+                        tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit->kvh * G, nit->q_start + nit->q0);
+                        if (nit->has1)
+                            tma_prefetch_l2_3d(&p.tmap_q, h * 64, nit->kvh * G,
+                                               nit->q_start + nit->q0 + T);
                     }
                 }
-                if (pub < loaded + kAhead && (cur >= 0 || mine != 0 || scan < n_pairs)) {
-                    if (cur < 0 && mine == 0) {
-                        // Scan 32 pairs: the kv heads of a pair are all valid or none.
-                        const int pp = scan + lane;
-                        const bool v = pp < n_pairs &&
-                                       get_item<PREFIX>(p, pp * Hkv,
-                                                        static_cast<uint32_t>(pp) % P == cta).valid;
-                        const uint32_t vm = __ballot_sync(0xffffffffu, v);
-                        r0_lane = vrank + static_cast<uint32_t>(Hkv) * __popc(vm & ((1u << lane) - 1u));
-                        // Does one of this CTA's ranks fall in [r0, r0 + Hkv)?  Only the
-                        // first two rounds from r0 / P can hold the first one.
-                        bool own = false;
-                        if (v) {
-                            const uint32_t r = r0_lane / P;
-                            const uint32_t t0 = target(r), t1 = target(r + 1);
-                            own = (t0 >= r0_lane && t0 < r0_lane + Hkv) || t1 < r0_lane + Hkv;
-                        }
-                        mine = __ballot_sync(0xffffffffu, own);
-                        win = scan;
-                        scan += 32;
-                        vrank += static_cast<uint32_t>(Hkv) * __popc(vm);
-                        continue;
-                    }
-                    if (cur < 0) {
-                        cur = __ffs(mine) - 1;
-                        mine &= mine - 1u;
-                        cur_r0 = __shfl_sync(0xffffffffu, r0_lane, cur);
-                        cur_round = cur_r0 / P;
-                    }
-                    const uint32_t tv = target(cur_round++);
-                    if (tv < cur_r0) continue;
-                    if (tv >= cur_r0 + Hkv) {
-                        cur = -1;
-                        continue;
-                    }
-                    const int idx = (win + cur) * Hkv + static_cast<int>(tv - cur_r0);
-                    if (lane == 0) {
-                        const Item it = get_item<PREFIX>(p, idx, false);
-                        if (pub >= kRing && !wait1(bar(B_IEMPTY + pub % kRing),
-                                                   ((pub / kRing) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
-                            ok = false;
-                        } else {
-                            info[pub % kRing].it = it;
-                            info[pub % kRing].end = 0;
-                            mbar_arrive(bar(B_IFULL + pub % kRing));
-                        }
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    ++pub;
-                    continue;
-                }
-                if (loaded == pub) break;  // the list is exhausted and every Q loaded
-                // Only a Q load can make progress: wait for its buffer.
-                if (lane == 0) ok = wait1(bar(B_QEMPTY), (loaded - 1) & 1, abort_flag, p.err, p.wait_ns);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            // End of the list (never marked under the stall testing aid: every other role's
-            // first wait then runs out, with nothing in flight).
-            if (ok && lane == 0 && !*abort_flag && !p.stall &&
-                (pub < kRing ||
-                 wait1(bar(B_IEMPTY + pub % kRing), ((pub / kRing) - 1) & 1, abort_flag, p.err, p.wait_ns))) {
-                info[pub % kRing].end = 1;
-                mbar_arrive(bar(B_IFULL + pub % kRing));
-            }
+            };
+            schedule_items<PREFIX>(p, info, bar(B_IFULL), bar(B_IEMPTY), abort_flag, gridDim.x,
+                                   blockIdx.x, true, q_free, q_wait, q_load);
         } else if (warp == kWarpK) {
             // ---------------- K producer (whole warp) ----------------
             if (lane == 0) prefetch_tmap(&p.tmap_k);
@@ -631,26 +657,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i == 0 && !wait1(bar(B_VFULL + gv % NSV), (gv / NSV) & 1, abort_flag, p.err, p.wait_ns))
                         return false;
                     tc_fence_after();
-                    const uint32_t vbase = sV + (gv % NSV) * L::TILE;
+                    const uint64_t b0 = smem_desc_sw128(sV + (gv % NSV) * L::TILE, HALF, 1024);
     #pragma unroll
                     for (int k = 0; k < KSTEPS_O; ++k) {
                         if (half && k >= KSTEPS_O / 2) break;
-                        const uint64_t b = smem_desc_sw128(vbase + k * 2048, HALF, 1024);
-                        mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, b, idesc_o,
-                                    (!first || k > 0) ? 1u : 0u);
+                        mma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + k * 8, desc_advance(b0, k * 2048),
+                                    idesc_o, (!first || k > 0) ? 1u : 0u);
                     }
                     mma_commit(bar(B_ODONE + i));
                     return true;
                 };
                 auto issue_s = [&](int i, uint32_t gk, bool half) {
-                    const uint32_t qbase = sQ + i * L::TILE;
-                    const uint32_t kbase = sK + (gk % NSK) * L::TILE;
+                    const uint64_t a0 = smem_desc_sw128(sQ + i * L::TILE, 16, 1024);
+                    const uint64_t b0 = smem_desc_sw128(sK + (gk % NSK) * L::TILE, 16, 1024);
+                    const uint32_t id = half ? idesc_s_half : idesc_s;
     #pragma unroll
                     for (int k = 0; k < KSTEPS_S; ++k) {
                         const uint32_t off = (k >> 2) * HALF + (k & 3) * 32;
-                        const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                        mma_bf16_ss(tmem + col_s(i), a, b, half ? idesc_s_half : idesc_s, k > 0);
+                        mma_bf16_ss(tmem + col_s(i), desc_advance(a0, off), desc_advance(b0, off), id, k > 0);
                     }
                     mma_commit(bar(B_SFULL + i));
                 };

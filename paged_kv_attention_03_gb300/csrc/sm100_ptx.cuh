@@ -221,6 +221,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
     return d;
 }
 
+// The descriptor of the same layout `bytes` further on (a multiple of 16): only the start
+// address field moves, and it cannot carry out of its 14 bits (shared memory < 256 KB).  The
+// MMA issuer builds one descriptor per operand tile and advances it per k-step, so it spends
+// one add instead of a descriptor build on each MMA (it shares an SM sub-partition with two
+// busy softmax warps, and a slow issue leaves the tensor pipe idle).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+    return d + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 // b_mn_major: B is stored N-major (N contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major) {
