@@ -624,8 +624,10 @@ def main():
     if not args.no_cascade:
         cascade = _cascade_leg(pa, dev, rank, peaks, flush, stream, args)
     fp8 = None
+    fp8_prefill = None
     if not args.no_fp8:
         fp8 = _fp8_leg(pa, dev, rank, peaks, flush, stream, args, case, runner)
+        fp8_prefill = _fp8_prefill_leg(pa, dev, rank, peaks, flush, stream, args)
 
     long_dec = None
     if not args.no_long and args.workload != "long_decode":
@@ -680,6 +682,8 @@ def main():
         line["cascade"] = cascade
     if fp8 is not None:
         line["fp8_decode"] = fp8
+    if fp8_prefill is not None:
+        line["fp8_prefill"] = fp8_prefill
     if long_dec is not None:
         line["long_decode"] = long_dec
     if tiny is not None:
@@ -820,6 +824,33 @@ def _tiny_decode_leg(pa, dev, rank, peaks, flush, stream, args):
             "launches": runner.launches,
             "note": "median device time of one pa_decode call (store fused); the data fit "
                     "in L2, so a roofline fraction is not meaningful"}
+
+
+def _fp8_prefill_leg(pa, dev, rank, peaks, flush, stream, args):
+    """The varlen-prefill workload over an FP8 E4M3 cache (codes of the bf16 pool / 0.02;
+    the prompt tokens quantised into it by the call), TFLOP/s as the bf16 leg counts them."""
+    case = make_case(WORKLOADS["varlen_prefill"], seed=100 + rank, device=dev)
+    kv_scale = 0.02
+    k8 = (case.k_cache.float() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (case.v_cache.float() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    runner = PrefillRunner(case, dev)
+    c, w = case, case.workload
+
+    def step(store=True):
+        kw = dict(key=c.key, value=c.value, slot_mapping=runner.slots) if store else {}
+        pa.pa_varlen_prefill_fp8(c.q, k8, v8, runner.cu, runner.seq_lens, runner.bt,
+                                 c.max_query_len, c.max_seq_len, w.final_scale, kv_scale,
+                                 w.sliding_window, out=runner.out, **kw)
+
+    steps = max(20, args.steps // 10)
+    ms = statistics.mean(_time_steps(step, steps, 3, flush, stream))
+    attn = statistics.mean(_time_steps(lambda: step(False), steps, 3, flush, stream))
+    return {"workload": "varlen_prefill over an E4M3 cache (kv_scale 0.02)",
+            "ms_per_step": round(ms, 4), "tflops": round(runner.work / (ms / 1e3) / 1e12, 2),
+            "attention_ms": round(attn, 4),
+            "attention_tflops": round(runner.work / (attn / 1e3) / 1e12, 2),
+            "frac_of_bf16_peak": round(runner.work / (attn / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+            "note": "f16 products on codes expanded in shared memory; FLOPs of the bf16 leg"}
 
 
 def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):

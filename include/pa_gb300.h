@@ -352,6 +352,27 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
                             int sliding_window, float scale, void *stream);
 
 /*
+ * pa_varlen_prefill_fp8 - pa_varlen_prefill over an FP8 E4M3 cache (the reading of the
+ * FP8 block above: the caches hold codes of x / kv_scale, attention reads code *
+ * kv_scale).  "05 Attention Backends", section 5: the backend views the cache as FP8 and
+ * hands that view to the one varlen call that serves prefill and decode rows.
+ * Arguments as pa_varlen_prefill, with k_cache / v_cache [num_blocks, block_size,
+ * num_kv_heads, head_dim] bytes, key / value (optional) stored as pa_store_kvcache_fp8,
+ * and kv_scale > 0 finite.  The products run in f16 (every E4M3 value is an f16; q is
+ * rounded to f16 once, exactly for |q| in [2^-14, 65504], clamped beyond 65504; the
+ * softmax weights are f16).  Supported: head_dim 128 (others: PA_ERR_UNSUPPORTED);
+ * single-row sequences go to the FP8 decode kernel as in pa_varlen_prefill.
+ */
+pa_status pa_varlen_prefill_fp8(void *out, const void *q, const void *key, const void *value,
+                                const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                const int32_t *seq_lens, const int32_t *block_table,
+                                int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
+                                int max_seqlen_k, int64_t num_blocks, int block_size,
+                                int num_heads, int num_kv_heads, int head_dim,
+                                int sliding_window, float scale, float kv_scale, void *stream);
+
+/*
  * pa_read_device_error - synchronise `stream`, then return in *flags the device
  * error word of the current device (PA_DEVERR_* bits OR-ed by every launch since it
  * was last cleared) and clear it when `clear` is non-zero.  Returns PA_OK when no

@@ -39,6 +39,7 @@ from ._lib import (  # noqa: F401
     pa_debug_prefill_stall,
     pa_store_kvcache,
     pa_varlen_prefill,
+    pa_varlen_prefill_fp8,
     status_string,
     version,
 )

@@ -34,7 +34,8 @@ EXPORTED = ("pa_status_string", "pa_version", "pa_store_kvcache", "pa_decode_num
             "pa_read_device_error", "pa_decode_noalloc", "pa_last_cuda_error_string",
             "pa_decode_state_workspace_size", "pa_decode_state", "pa_merge_states",
             "pa_cascade_decode_workspace_size", "pa_cascade_decode", "pa_common_prefix_blocks",
-            "pa_store_kvcache_fp8", "pa_decode_fp8", "pa_debug_prefill_stall")
+            "pa_store_kvcache_fp8", "pa_decode_fp8", "pa_debug_prefill_stall",
+            "pa_varlen_prefill_fp8")
 
 
 class PAError(RuntimeError):
@@ -490,6 +491,52 @@ def pa_varlen_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                    int(max_seqlen_k), nb, bs, num_heads, hkv, head_dim,
                                    int(sliding_window), float(scale), _stream(dev))
     _check(st, "pa_varlen_prefill")
+    return out
+
+
+def pa_varlen_prefill_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor | None,
+                          block_table: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                          scale: float, kv_scale: float, sliding_window: int = 0,
+                          cu_seqlens_k: torch.Tensor | None = None,
+                          key: torch.Tensor | None = None, value: torch.Tensor | None = None,
+                          slot_mapping: torch.Tensor | None = None,
+                          out: torch.Tensor | None = None) -> torch.Tensor:
+    """pa_varlen_prefill over FP8 E4M3 caches (uint8 [NB, bs, Hkv, D], read as code *
+    kv_scale); q / key / value / out bf16.  New tokens, when given, are quantised into the
+    caches first."""
+    lib = load()
+    fn = lib.pa_varlen_prefill_fp8
+    if fn.restype is not ctypes.c_int or fn.argtypes is None:
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64,
+                       i32, i32, i32, i32, i32, f32, f32, vp]
+        fn.restype = ctypes.c_int
+    dev = q.device
+    _need(q, torch.bfloat16, "q", dev)
+    _need(k_cache, torch.uint8, "k_cache", dev)
+    _need(v_cache, torch.uint8, "v_cache", dev)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    if seq_lens is not None:
+        _need(seq_lens, torch.int32, "seq_lens", dev)
+    if cu_seqlens_k is not None:
+        _need(cu_seqlens_k, torch.int32, "cu_seqlens_k", dev)
+    total_q, num_heads, head_dim = q.shape
+    nb, bs, hkv, d = k_cache.shape
+    num_seqs = cu_seqlens_q.shape[0] - 1
+    if (d != head_dim or v_cache.shape != k_cache.shape or block_table.dim() != 2
+            or block_table.shape[0] != num_seqs):
+        raise ValueError("pa_varlen_prefill_fp8: inconsistent shapes")
+    _new_tokens(key, value, slot_mapping, total_q, hkv, head_dim, dev, "pa_varlen_prefill_fp8")
+    out = _out(out, q.shape, torch.bfloat16, dev)
+    with _on(dev):
+        st = fn(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+                _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(seq_lens),
+                _ptr(block_table), block_table.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                int(max_seqlen_k), nb, bs, num_heads, hkv, head_dim, int(sliding_window),
+                float(scale), float(kv_scale), _stream(dev))
+    _check(st, "pa_varlen_prefill_fp8")
     return out
 
 

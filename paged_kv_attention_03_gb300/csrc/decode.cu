@@ -142,38 +142,6 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-// Four FP8 E4M3 codes (low byte first) -> two f16x2 words, exactly (every E4M3 value, at
-// most 4 significant bits with exponents 2^-9 .. 2^8, is an f16): codes 0, 1 into lo and
-// codes 2, 3 into hi.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
-    asm("{\n"
-        ".reg .b16 a, b;\n"
-        "mov.b32 {a, b}, %2;\n"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n"
-        "cvt.rn.f16x2.e4m3x2 %1, b;\n"
-        "}\n"
-        : "=r"(lo), "=r"(hi)
-        : "r"(four));
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    uint32_t h;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
-    return h;
-}
-
-// lo += float(f16 low half of v), hi += float(f16 high half of v) (mixed-precision adds).
-__device__ __forceinline__ void add_f16x2_f32(float &lo, float &hi, uint32_t v) {
-    asm("{\n"
-        ".reg .b16 l, h;\n"
-        "mov.b32 {l, h}, %2;\n"
-        "add.rn.f32.f16 %0, l, %0;\n"
-        "add.rn.f32.f16 %1, h, %1;\n"
-        "}\n"
-        : "+f"(lo), "+f"(hi)
-        : "r"(v));
-}
-
 // Transpose of an 8x8 matrix of 16-bit elements held as the MMA accumulator fragment
 // (lane holds row lane/4, columns 2 (lane%4) and + 1): afterwards the lane holds row
 // lane/4 of the transpose.
@@ -358,11 +326,7 @@ __device__ __forceinline__ void decode_split_body(const DecodeKernelParams &p) {
             // k 2t+8, 2t+9 dims 4t+2, 4t+3 of the step (t = lane % 4).  |q| is clamped
             // to the f16 range.
             const int c0 = (lane & 3) * 4;
-            auto f16pair = [](uint32_t w) -> uint32_t {
-                const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
-                const float hi = fminf(fmaxf(__uint_as_float(w & 0xffff0000u), -65504.f), 65504.f);
-                return pack_f16x2(lo, hi);
-            };
+            auto f16pair = [](uint32_t w) -> uint32_t { return bf16x2_to_f16x2(w); };
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll

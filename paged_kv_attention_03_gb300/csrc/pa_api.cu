@@ -469,14 +469,18 @@ pa_status pa_merge_states(void *out, float *out_state, float *out_lse, const flo
     return from_cuda(pa::launch_merge_states(a, static_cast<cudaStream_t>(stream)));
 }
 
-pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
-                            const int32_t *slot_mapping, void *k_cache, void *v_cache,
-                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                            const int32_t *seq_lens, const int32_t *block_table,
-                            int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
-                            int max_seqlen_k, int64_t num_blocks, int block_size,
-                            int num_heads, int num_kv_heads, int head_dim,
-                            int sliding_window, float scale, void *stream) {
+namespace {
+
+// pa_varlen_prefill and pa_varlen_prefill_fp8: argument checks, the optional store of the
+// new tokens, then the launch.
+pa_status varlen_prefill(void *out, const void *q, const void *key, const void *value,
+                         const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                         const int32_t *seq_lens, const int32_t *block_table, int max_num_blocks,
+                         int num_seqs, int total_q, int max_seqlen_q, int max_seqlen_k,
+                         int64_t num_blocks, int block_size, int num_heads, int num_kv_heads,
+                         int head_dim, int sliding_window, float scale, void *stream, bool fp8,
+                         float kv_scale) {
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         num_blocks < 0 || max_num_blocks < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || block_size <= 0)
@@ -484,7 +488,8 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (max_seqlen_q > max_seqlen_k) return PA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !(scale < 3.0e38f)) return PA_ERR_INVALID_ARG;  // folded into exp2
-    if (!supported_head_dim(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (fp8 && (!(kv_scale > 0.f) || !(kv_scale < 3.0e38f))) return PA_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || (fp8 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 128) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per sequence
@@ -499,12 +504,13 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
     if (max_seqlen_k > 0 && max_num_blocks == 0) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (has_new) {
-        const pa_status st = check_store(key, value, k_cache, v_cache, slot_mapping, total_q,
-                                         num_blocks, block_size, num_kv_heads, head_dim);
+        const pa_status st = fp8 ? pa_store_kvcache_fp8(key, value, k_cache, v_cache, slot_mapping,
+                                                        total_q, num_blocks, block_size,
+                                                        num_kv_heads, head_dim, kv_scale, stream)
+                                 : pa_store_kvcache(key, value, k_cache, v_cache, slot_mapping,
+                                                    total_q, num_blocks, block_size,
+                                                    num_kv_heads, head_dim, stream);
         if (st != PA_OK) return st;
-        const pa_status rs = run_store(key, value, k_cache, v_cache, slot_mapping, total_q,
-                                       num_blocks, block_size, num_kv_heads, head_dim, s);
-        if (rs != PA_OK) return rs;
     }
     pa::PrefillArgs a{};
     a.out = out;
@@ -527,8 +533,40 @@ pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const voi
     a.head_dim = head_dim;
     a.sliding_window = sliding_window;
     a.scale = scale;
+    a.fp8 = fp8 ? 1 : 0;
+    a.kv_scale = kv_scale;
     a.err = device_error_word();
     return from_cuda(pa::launch_prefill(a, s));
+}
+
+}  // namespace
+
+pa_status pa_varlen_prefill(void *out, const void *q, const void *key, const void *value,
+                            const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *seq_lens, const int32_t *block_table,
+                            int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
+                            int max_seqlen_k, int64_t num_blocks, int block_size,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int sliding_window, float scale, void *stream) {
+    return varlen_prefill(out, q, key, value, slot_mapping, k_cache, v_cache, cu_seqlens_q,
+                          cu_seqlens_k, seq_lens, block_table, max_num_blocks, num_seqs, total_q,
+                          max_seqlen_q, max_seqlen_k, num_blocks, block_size, num_heads,
+                          num_kv_heads, head_dim, sliding_window, scale, stream, false, 1.f);
+}
+
+pa_status pa_varlen_prefill_fp8(void *out, const void *q, const void *key, const void *value,
+                                const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                const int32_t *seq_lens, const int32_t *block_table,
+                                int max_num_blocks, int num_seqs, int total_q, int max_seqlen_q,
+                                int max_seqlen_k, int64_t num_blocks, int block_size,
+                                int num_heads, int num_kv_heads, int head_dim,
+                                int sliding_window, float scale, float kv_scale, void *stream) {
+    return varlen_prefill(out, q, key, value, slot_mapping, k_cache, v_cache, cu_seqlens_q,
+                          cu_seqlens_k, seq_lens, block_table, max_num_blocks, num_seqs, total_q,
+                          max_seqlen_q, max_seqlen_k, num_blocks, block_size, num_heads,
+                          num_kv_heads, head_dim, sliding_window, scale, stream, true, kv_scale);
 }
 
 pa_status pa_debug_prefill_stall(int stall, uint64_t wait_limit_ns) {

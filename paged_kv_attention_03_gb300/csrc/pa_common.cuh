@@ -69,6 +69,46 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four FP8 E4M3 codes (low byte first) -> two f16x2 words, exactly (every E4M3 value, at
+// most 4 significant bits with exponents 2^-9 .. 2^8, is an f16): codes 0, 1 into lo and
+// codes 2, 3 into hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    asm("{\n"
+        ".reg .b16 a, b;\n"
+        "mov.b32 {a, b}, %2;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n"
+        "}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// Two bf16 (low half first) -> two f16: exact for values in the f16 normal range, rounded
+// below it, clamped to +-65504 beyond it.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
+    const float hi = fminf(fmaxf(__uint_as_float(w & 0xffff0000u), -65504.f), 65504.f);
+    return pack_f16x2(lo, hi);
+}
+
+// lo += float(f16 low half of v), hi += float(f16 high half of v) (mixed-precision adds).
+__device__ __forceinline__ void add_f16x2_f32(float &lo, float &hi, uint32_t v) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %2;\n"
+        "add.rn.f32.f16 %0, l, %0;\n"
+        "add.rn.f32.f16 %1, h, %1;\n"
+        "}\n"
+        : "+f"(lo), "+f"(hi)
+        : "r"(v));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

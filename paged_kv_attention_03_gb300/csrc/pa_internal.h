@@ -128,6 +128,9 @@ struct PrefillArgs {
     int head_dim;
     int sliding_window;
     float scale;
+    // FP8 E4M3 cache (head_dim 128): k_cache / v_cache hold codes of x / kv_scale.
+    int fp8;
+    float kv_scale;
     unsigned *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -45,6 +45,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -117,6 +118,7 @@ struct PrefillKernelParams {
     int chunk_tiles;
     // Sequences with one query row are left to the decode kernel of the same call.
     int skip_decode_rows;
+    float kv_scale;    // FP8 cache: attention reads code * kv_scale (folded into scale_log2 for K)
     uint64_t wait_ns;  // limit of every wait (kTimeoutNs unless a test lowers it)
     int stall;         // testing aid: publish no work item, so every wait runs out
     unsigned *err;
@@ -135,7 +137,12 @@ enum : int {
     B_ODONE = B_PFULL + 2,     // [2]
     B_IFULL = B_ODONE + 2,       // [kRing]: item-info ring slot written
     B_IEMPTY = B_IFULL + kRing,  // [kRing]: slot read by every consumer
-    NBARS = B_IEMPTY + kRing
+    // FP8 cache: the codes of a K / V tile landed (before their conversion to f16), and
+    // both query tiles converted to f16 by the softmax warps.
+    B_LK = B_IEMPTY + kRing,     // [NSK]
+    B_LV = B_LK + NSK,           // [NSV]
+    B_QCONV = B_LV + NSV,
+    NBARS = B_QCONV + 1
 };
 
 template <int HD>
@@ -445,6 +452,15 @@ __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *w) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -452,9 +468,44 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-template <int HD, bool PREFIX>
+// One 128-key tile of E4M3 codes, [128 rows][128 codes] row-major in the upper half of a
+// stage, expanded in place into the f16 operand layout of the stage ([128][64] per 64-dim
+// half, 128-byte swizzle), by one whole warp (4 rows a lane).  A row's f16 output of its
+// upper half shares its 128-byte line with the row's own codes only, and the lane reads
+// all of them before it writes, so no lane overwrites codes another lane still needs.
+__device__ __forceinline__ void convert_tile_e4m3(uint32_t stage, int lane) {
+    constexpr uint32_t kCodes = 128u * 128u;  // the f16 tile is 32 KB; its codes sit at 16 KB
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t r = static_cast<uint32_t>(lane + 32 * i);
+        uint4 c[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c[j] = ld_shared_v4(stage + kCodes + r * 128u + j * 16u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // codes of head dims 16 j .. 16 j + 15: 64-dim half j / 4, 16-byte chunks 2 (j % 4)
+            // and 2 (j % 4) + 1 of row r
+            uint32_t w[8];
+            e4m3x4_to_f16x2x2(c[j].x, w[0], w[1]);
+            e4m3x4_to_f16x2x2(c[j].y, w[2], w[3]);
+            e4m3x4_to_f16x2x2(c[j].z, w[4], w[5]);
+            e4m3x4_to_f16x2x2(c[j].w, w[6], w[7]);
+            const uint32_t line = stage + (j >> 2) * HALF + r * 128u;
+            const uint32_t c0 = 2u * (j & 3);
+            st_shared_v4(line + ((c0 ^ (r & 7u)) << 4), w[0], w[1], w[2], w[3]);
+            st_shared_v4(line + (((c0 + 1u) ^ (r & 7u)) << 4), w[4], w[5], w[6], w[7]);
+        }
+    }
+}
+
+// FP8: the cache holds E4M3 codes (head_dim 128).  The producers TMA-load a tile's codes into
+// the upper half of its shared-memory stage and expand them in place to f16 in the MMA
+// operand layout (every E4M3 value is an f16); the softmax warps convert each query tile
+// to f16 in place; the products are f16 MMAs with P in f16.
+template <int HD, bool PREFIX, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillKernelParams p) {
+    static_assert(!FP8 || (HD == 128 && !PREFIX), "the FP8 cache path is built for head_dim 128");
     using L = Layout<HD>;
     constexpr int NHALF = L::NHALF;
     constexpr int KSTEPS_S = HD / 16;  // MMAs per S tile
@@ -503,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_IFULL + i), 1);
             mbar_init(bar(B_IEMPTY + i), kConsumersPerItem);
         }
+        for (int s = 0; s < NSK; ++s) mbar_init(bar(B_LK + s), 1);
+        for (int s = 0; s < NSV; ++s) mbar_init(bar(B_LV + s), 1);
+        mbar_init(bar(B_QCONV), 8);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -594,55 +648,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             schedule_items<PREFIX>(p, info, bar(B_IFULL), bar(B_IEMPTY), abort_flag, gridDim.x,
                                    blockIdx.x, true, q_free, q_wait, q_load);
-        } else if (warp == kWarpK) {
-            // ---------------- K producer (whole warp) ----------------
-            if (lane == 0) prefetch_tmap(&p.tmap_k);
-            uint32_t t = 0;
+        } else if (warp == kWarpK || warp == kWarpV) {
+            // ---------------- K / V producer (whole warp) ----------------
+            auto produce = [&](auto is_k_tag) {
+            constexpr bool is_k = decltype(is_k_tag)::value;
+            const CUtensorMap *map = is_k ? &p.tmap_k : &p.tmap_v;
+            const uint32_t sbase = is_k ? sK : sV;
+            constexpr uint32_t NS = is_k ? NSK : NSV;
+            constexpr int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
+            if (lane == 0) prefetch_tmap(map);
+            uint32_t t = 0;  // tiles issued
             bool ok = true;
             Item it;
-            for (uint32_t ic = 0; ok && take_item(ic, it); ++ic) {
-                for (int j = 0; j < it.n_tiles; ++j, ++t) {
-                    const int st = t % NSK;
-                    if (t >= NSK &&
-                        !wait_warp(bar(B_KEMPTY + st), ((t / NSK) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
-                        ok = false;
-                        break;
+            if constexpr (!FP8) {
+                for (uint32_t ic = 0; ok && take_item(ic, it); ++ic) {
+                    for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                        const uint32_t st = t % NS;
+                        if (t >= NS && !wait_warp(bar(b_empty + st), ((t / NS) - 1) & 1, abort_flag,
+                                                  p.err, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) mbar_arrive_expect_tx(bar(b_full + st), L::TILE);
+                        __syncwarp();
+                        load_kv(map, it, (it.kt0 + j) * BN, sbase + st * L::TILE, bar(b_full + st));
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), L::TILE);
-                    __syncwarp();
-                    load_kv(&p.tmap_k, it, (it.kt0 + j) * BN, sK + st * L::TILE, bar(B_KFULL + st));
                 }
-            }
-        } else if (warp == kWarpV) {
-            // ---------------- V producer (whole warp) ----------------
-            if (lane == 0) prefetch_tmap(&p.tmap_v);
-            uint32_t t = 0;
-            bool ok = true;
-            Item it;
-            for (uint32_t ic = 0; ok && take_item(ic, it); ++ic) {
-                for (int j = 0; j < it.n_tiles; ++j, ++t) {
-                    const int st = t % NSV;
-                    if (t >= NSV &&
-                        !wait_warp(bar(B_VEMPTY + st), ((t / NSV) - 1) & 1, abort_flag, p.err, p.wait_ns)) {
-                        ok = false;
-                        break;
+            } else {
+                // The codes of tile t land in the upper half of its stage (barrier B_LK / B_LV);
+                // the warp converts tile t - (NS - 1) once tile t is issued, so NS - 1 tiles of
+                // codes are in flight while it converts, and converts what is pending while
+                // the next item is not yet published.
+                constexpr int b_land = is_k ? B_LK : B_LV;
+                uint32_t tc = 0;  // tiles converted
+                auto convert_next = [&]() -> bool {
+                    const uint32_t st = tc % NS;
+                    if (!wait_warp(bar(b_land + st), (tc / NS) & 1, abort_flag, p.err, p.wait_ns))
+                        return false;
+                    convert_tile_e4m3(sbase + st * L::TILE, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(b_full + st));
+                    ++tc;
+                    return true;
+                };
+                for (uint32_t ic = 0; ok; ++ic) {
+                    while (ok && tc < t &&
+                           !__all_sync(0xffffffffu, mbar_test_wait(bar(B_IFULL + ic % kRing), (ic / kRing) & 1)))
+                        ok = convert_next();
+                    if (!ok || !take_item(ic, it)) break;
+                    for (int j = 0; j < it.n_tiles; ++j) {
+                        const uint32_t st = t % NS;
+                        if (t >= NS && !wait_warp(bar(b_empty + st), ((t / NS) - 1) & 1, abort_flag,
+                                                  p.err, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) mbar_arrive_expect_tx(bar(b_land + st), L::TILE / 2);
+                        __syncwarp();
+                        if (lane < BN / 16) {  // one 16-key piece of codes per lane
+                            const int row = kv_row(it, (it.kt0 + j) * BN + 16 * lane);
+                            tma_load_3d(sbase + st * L::TILE + L::TILE / 2 + lane * 2048, map, 0, it.kvh,
+                                        row, bar(b_land + st));
+                        }
+                        ++t;
+                        while (ok && t - tc > NS - 1) ok = convert_next();
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), L::TILE);
-                    __syncwarp();
-                    load_kv(&p.tmap_v, it, (it.kt0 + j) * BN, sV + st * L::TILE, bar(B_VFULL + st));
                 }
+                while (ok && tc < t) ok = convert_next();
             }
+            };
+            if (warp == kWarpK)
+                produce(std::true_type{});
+            else
+                produce(std::false_type{});
         } else if (warp == kWarpMma) {
             // ---------------- MMA issuer ----------------
             // Order on the tensor pipe, across items: P0 V(g-1), S0(g), P1 V(g-1), S1(g).
             if (lane == 0) {
-                constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+                constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, FP8);
                 // Half tile: the item's last K/V tile when no row sees its upper 64 keys
                 // (diagonal of a query block that ends in the tile's lower half): S over
                 // 64 keys, P V over 64 keys.  The softmax needs no change: the causal mask
                 // already sets columns 64..127 to -inf.
-                constexpr uint32_t idesc_s_half = idesc_bf16_f32(BM, BN / 2, false);
-                constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true);
+                constexpr uint32_t idesc_s_half = idesc_bf16_f32(BM, BN / 2, false, FP8);
+                constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, true, FP8);
                 uint32_t g = 0;                  // global KV tile counter
                 uint32_t cnt[2] = {0, 0};        // tiles issued per query tile (S / P V)
                 uint32_t ic = 0;                 // items
@@ -698,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (end) break;
                     // Finish the previous item before waiting for this item's Q, so its
                     // epilogue never waits on a Q load.
-                    if (!flush() || !wait1(bar(B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) {
+                    if (!flush() || !wait1(bar(FP8 ? B_QCONV : B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -761,6 +851,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_IEMPTY + ic % kRing));
             if (end) break;
+            if constexpr (FP8) {
+                // The item's query tiles to f16, in place (a thread converts its row; the
+                // 16-byte chunks of a row share its 128-byte line whatever the swizzle).  Both
+                // warpgroups wait for the item's Q load even when tile 1 has no rows, so
+                // neither arrives on QCONV for a later item before this one's phase is done.
+                if (!wait_warp(bar(B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) break;
+                if (wg == 0 || it.has1) {
+                    if (row_in_tile) {
+#pragma unroll
+                        for (int h = 0; h < NHALF; ++h)
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint32_t a = sQ + wg * L::TILE + h * HALF + row * 128 + c8 * 16;
+                                const uint4 v = ld_shared_v4(a);
+                                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                             bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                            }
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_QCONV));
+            }
             if (wg == 1 && !it.has1) {
                 gt += it.n_tiles;
                 continue;
@@ -865,8 +978,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   sl2x2, negm2);
                         float x0, x1;
                         f2_unpack(x, x0, x1);
-                        pk[i] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-                        add_bf16x2_f32(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], pk[i]);
+                        if constexpr (FP8) {
+                            pk[i] = pack_f16x2(ex2_approx(x0), ex2_approx(x1));
+                            add_f16x2_f32(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], pk[i]);
+                        } else {
+                            pk[i] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+                            add_bf16x2_f32(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], pk[i]);
+                        }
                     }
                     tmem_st_32x32b_x32_u(scol + cc * 32, pk);
                 }
@@ -903,7 +1021,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            // (FP8: V elements are code * kv_scale.)
+            const float inv = l_sum > 0.f ? (FP8 ? p.kv_scale : 1.f) / l_sum : 0.f;
             if constexpr (PREFIX) {
                 // Partial state of this key split: fp32 row and ln of its denominator.
                 const int64_t rows = static_cast<int64_t>(p.num_req) * p.num_heads;
@@ -1057,17 +1176,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2) {
+               uint32_t b2, bool codes = false) {
     auto fn = get_encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // codes: one-byte FP8 codes, rows copied as they are (no swizzle)
+    const CUresult r = fn(map, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1084,20 +1205,23 @@ int sm_count() {
     return n;
 }
 
-template <int HD, bool PREFIX>
+template <int HD, bool PREFIX, bool FP8 = false>
 cudaError_t launch_prefill_d(PrefillKernelParams &kp, const PrefillArgs &a, cudaStream_t stream) {
     using L = Layout<HD>;
     const int64_t slots = a.num_blocks * a.block_size;
     if (!encode_3d(&kp.tmap_q, a.q, HD, a.num_heads, a.total_q, HD * 2ull,
                    static_cast<uint64_t>(a.num_heads) * HD * 2ull, 64, kp.group, kp.tok_per_tile))
         return cudaErrorInvalidValue;
-    if (!encode_3d(&kp.tmap_k, a.k_cache, HD, a.num_kv_heads, static_cast<uint64_t>(slots),
-                   HD * 2ull, static_cast<uint64_t>(a.num_kv_heads) * HD * 2ull, 64, 1, 16))
-        return cudaErrorInvalidValue;
-    if (!encode_3d(&kp.tmap_v, a.v_cache, HD, a.num_kv_heads, static_cast<uint64_t>(slots),
-                   HD * 2ull, static_cast<uint64_t>(a.num_kv_heads) * HD * 2ull, 64, 1, 16))
-        return cudaErrorInvalidValue;
-    auto kern = prefill_kernel<HD, PREFIX>;
+    // K / V boxes: one 16-row piece of a page and a 64-dim half (bf16), or the piece's whole
+    // rows of codes (FP8).
+    const uint64_t eb = FP8 ? 1ull : 2ull;  // bytes per cache element
+    for (int kv = 0; kv < 2; ++kv) {
+        if (!encode_3d(kv ? &kp.tmap_v : &kp.tmap_k, kv ? a.v_cache : a.k_cache, HD,
+                       a.num_kv_heads, static_cast<uint64_t>(slots), HD * eb,
+                       static_cast<uint64_t>(a.num_kv_heads) * HD * eb, FP8 ? HD : 64, 1, 16, FP8))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = prefill_kernel<HD, PREFIX, FP8>;
     static std::atomic<uint64_t> smem_set;
     cudaError_t e = smem_limit_once(kern, static_cast<int>(L::SMEM), smem_set);
     if (e != cudaSuccess) return e;
@@ -1145,7 +1269,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
     kp.n_items = static_cast<int>(n_items);
     kp.window = a.sliding_window;
-    kp.scale_log2 = a.scale * kLog2e;
+    kp.kv_scale = a.fp8 ? a.kv_scale : 1.f;
+    kp.scale_log2 = a.scale * kp.kv_scale * kLog2e;  // FP8: K elements are code * kv_scale
     kp.err = a.err;
     set_launch_limits(kp);
     // Sequences with a single query row (decode rows of a mixed batch) would fill one
@@ -1156,10 +1281,15 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     const bool prefill_launched = !route || a.max_seqlen_q > 1;
     if (prefill_launched) {
         cudaError_t e;
-        switch (a.head_dim) {
-            case 64: e = launch_prefill_d<64, false>(kp, a, stream); break;
-            case 128: e = launch_prefill_d<128, false>(kp, a, stream); break;
-            default: return cudaErrorInvalidValue;
+        if (a.fp8) {
+            if (a.head_dim != 128) return cudaErrorInvalidValue;
+            e = launch_prefill_d<128, false, true>(kp, a, stream);
+        } else {
+            switch (a.head_dim) {
+                case 64: e = launch_prefill_d<64, false>(kp, a, stream); break;
+                case 128: e = launch_prefill_d<128, false>(kp, a, stream); break;
+                default: return cudaErrorInvalidValue;
+            }
         }
         if (e != cudaSuccess || !route) return e;
     }
@@ -1189,6 +1319,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     d.check_rows = !prefill_launched;
     d.max_seqlen_q = a.max_seqlen_q;
     d.cu_seqlens_k = a.cu_seqlens_k;
+    d.fp8 = a.fp8;
+    d.kv_scale = a.kv_scale;
     d.after_prefill = prefill_launched;
     d.err = a.err;
     return launch_decode(d, plan, stream);

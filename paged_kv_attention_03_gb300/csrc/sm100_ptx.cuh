@@ -230,12 +230,13 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
     return d + static_cast<uint64_t>(bytes >> 4);
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
-// b_mn_major: B is stored N-major (N contiguous) instead of K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major) {
+// Instruction descriptor for tcgen05.mma kind::f16 with bf16 A/B (f16 A/B when f16) and
+// fp32 D.  b_mn_major: B is stored N-major (N contiguous) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major,
+                                                      bool f16 = false) {
     return (1u << 4)                                    // D format: f32
-           | (1u << 7)                                  // A format: bf16
-           | (1u << 10)                                 // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)                     // A format: bf16 (1) or f16 (0)
+           | ((f16 ? 0u : 1u) << 10)                    // B format: likewise
            | (0u << 15)                                 // A K-major
            | ((b_mn_major ? 1u : 0u) << 16)             // B major-ness
            | (static_cast<uint32_t>(n >> 3) << 17)      // N / 8

@@ -87,7 +87,10 @@ def assert_parity(got: torch.Tensor, ref: np.ndarray, what: str = "",
     2. against the oracle rounded once to the output type: max-abs <= max_abs, except
        where that type's spacing exceeds max_abs (|ref| >= 2 for bf16), where the output
        must be the correctly rounded value or one of its two neighbours.
-    The mean-abs bar is against the fp64 oracle."""
+    The mean-abs bar is taken against the oracle rounded once to the output type: the
+    rounding of the output itself (about a quarter of an ulp on average, ~1e-3 for rows of
+    magnitude ~1, as a window of one key over an FP8 cache gives) is not arithmetic error.
+    Both mean-abs figures are reported."""
     g = got.detach().float().cpu().double().numpy()
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
@@ -101,6 +104,7 @@ def assert_parity(got: torch.Tensor, ref: np.ndarray, what: str = "",
              "mean_abs": float(err.mean()) if err.size else 0.0,
              "max_excess": float(excess.max()) if err.size else -max_abs,
              "max_abs_vs_rounded": float(err_r[~coarse].max()) if (~coarse).any() else 0.0,
+             "mean_abs_vs_rounded": float(err_r.mean()) if err.size else 0.0,
              "coarse_elems": int(coarse.sum()),
              "elems": int(err.size)}
     RECORDS.append((what, stats))
@@ -113,7 +117,8 @@ def assert_parity(got: torch.Tensor, ref: np.ndarray, what: str = "",
     if coarse.any():
         bad = err_r[coarse] > ulp[coarse] * 1.0000001
         assert not bad.any(), f"{what}: an output with |ref| >= 2 is more than one ulp off"
-    assert stats["mean_abs"] <= mean_abs, f"{what}: mean-abs {stats['mean_abs']:.3e} > {mean_abs}"
+    assert stats["mean_abs_vs_rounded"] <= mean_abs, \
+        f"{what}: mean-abs {stats['mean_abs_vs_rounded']:.3e} against the rounded oracle > {mean_abs}"
     return stats
 
 

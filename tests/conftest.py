@@ -43,4 +43,5 @@ def pytest_terminal_summary(terminalreporter):
     for w, st in full:
         terminalreporter.write_line(
             f"  {w}: {st['elems']} elems, max-abs {st['max_abs']:.2e}, mean-abs "
-            f"{st['mean_abs']:.2e}, max-abs vs bf16-rounded oracle {st['max_abs_vs_rounded']:.2e}")
+            f"{st['mean_abs']:.2e}; vs the bf16-rounded oracle max-abs "
+            f"{st['max_abs_vs_rounded']:.2e}, mean-abs {st['mean_abs_vs_rounded']:.2e}")

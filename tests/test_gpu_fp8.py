@@ -101,3 +101,97 @@ def test_fp8_decode_with_fused_store(cuda):
                                      case.seq_lens, case.block_table, 32, 8, 0,
                                      case.workload.final_scale, s)
     assert_parity(out, ref, "fp8 fused store")
+
+
+# ----------------------------------------------------------------- varlen prefill ---
+
+def _fp8_prefill_case(dev, ctx, qlens, H=32, Hkv=8, bs=16, seed=110, kv_scale=0.02):
+    w = Workload("p8", H, Hkv, 128, bs, ())
+    case = make_case_from_lengths(w, ctx, qlens, seed=seed, device=dev)
+    return case, _codes_of(case.k_cache, kv_scale), _codes_of(case.v_cache, kv_scale), kv_scale
+
+
+def _fp8_prefill_check(case, kc, vc, s, dev, window=0, fused_store=False, what=""):
+    """pa_varlen_prefill_fp8 over the codes (optionally storing the step's tokens first)
+    against the FP8 oracle on every row."""
+    hk, hv = kc.copy(), vc.copy()
+    kw = {}
+    if fused_store:
+        oracle.store_kvcache_fp8(bf16_bits(case.key), bf16_bits(case.value), hk, hv,
+                                 case.slot_mapping, case.workload.block_size, s)
+        kw = dict(key=case.key, value=case.value, slot_mapping=_t(case.slot_mapping, dev))
+    dk, dv = torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev)
+    w = case.workload
+    out = pa.pa_varlen_prefill_fp8(case.q, dk, dv, _t(case.cu_seqlens_q, dev),
+                                   _t(case.seq_lens, dev), _t(case.block_table, dev),
+                                   case.max_query_len, case.max_seq_len, w.final_scale, s,
+                                   window, **kw)
+    flags = pa.pa_read_device_error(device=dev)
+    assert flags == 0, f"device error bits {flags:#x}"
+    if fused_store:
+        np.testing.assert_array_equal(dk.cpu().numpy(), hk)
+        np.testing.assert_array_equal(dv.cpu().numpy(), hv)
+    ref = oracle.paged_attention_fp8(bf16_bits(case.q), hk, hv, case.cu_seqlens_q,
+                                     case.seq_lens, case.block_table, w.num_heads,
+                                     w.num_kv_heads, window, w.final_scale, s)
+    return assert_parity(out, ref, what or f"fp8 prefill window={window}")
+
+
+@pytest.mark.parametrize("window", [0, 1, 100, 300])
+def test_fp8_prefill_windows_and_chunks(cuda, window):
+    case, kc, vc, s = _fp8_prefill_case(cuda, [0, 0, 37, 130, 500, 3], [1, 160, 64, 129, 31, 1])
+    _fp8_prefill_check(case, kc, vc, s, cuda, window=window)
+
+
+@pytest.mark.parametrize("lens", [[16], [127], [128], [129], [255], [257], [700]])
+def test_fp8_prefill_tile_edges(cuda, lens):
+    case, kc, vc, s = _fp8_prefill_case(cuda, [0] * len(lens), lens, seed=111, kv_scale=0.5)
+    _fp8_prefill_check(case, kc, vc, s, cuda)
+
+
+@pytest.mark.parametrize("H,Hkv,bs", [(8, 8, 16), (40, 8, 32), (16, 2, 64), (64, 4, 256)])
+def test_fp8_prefill_shapes(cuda, H, Hkv, bs):
+    case, kc, vc, s = _fp8_prefill_case(cuda, [0, 5, 100], [150, 17, 33], H=H, Hkv=Hkv, bs=bs,
+                                        seed=112, kv_scale=0.1)
+    _fp8_prefill_check(case, kc, vc, s, cuda)
+    _fp8_prefill_check(case, kc, vc, s, cuda, window=50)
+
+
+def test_fp8_prefill_many_sequences(cuda):
+    rng = np.random.default_rng(8)
+    q = rng.integers(1, 301, size=150)
+    ctx = np.where(rng.random(150) < 0.3, rng.integers(0, 200, size=150), 0)
+    case, kc, vc, s = _fp8_prefill_case(cuda, ctx, q, seed=113)
+    _fp8_prefill_check(case, kc, vc, s, cuda)
+
+
+def test_fp8_mixed_batch_with_store(cuda):
+    # Chunks with a cached context and single-row decodes in one call over an FP8 cache; the
+    # call quantises the step's new tokens into the cache first.
+    case, kc, vc, s = _fp8_prefill_case(cuda, [1000, 0, 37, 4000, 9, 600],
+                                        [512, 300, 1, 1, 1, 200], seed=114, kv_scale=0.05)
+    _fp8_prefill_check(case, kc, vc, s, cuda, window=0, fused_store=True, what="fp8 mixed")
+    _fp8_prefill_check(case, kc, vc, s, cuda, window=700, fused_store=True,
+                       what="fp8 mixed window")
+
+
+def test_fp8_prefill_rejects_head_dim_64(cuda):
+    w = Workload("p8d64", 8, 2, 64, 16, ())
+    case = make_case_from_lengths(w, [0], [40], seed=115, device=cuda)
+    kc = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device=cuda)
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_varlen_prefill_fp8(case.q, kc, kc.clone(), _t(case.cu_seqlens_q, cuda),
+                                 _t(case.seq_lens, cuda), _t(case.block_table, cuda), 40, 40,
+                                 w.final_scale, 0.1)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+def test_fp8_prefill_full_size_varlen(cuda):
+    # The varlen-prefill workload (16 prompts of U[128, 2048], 32/8 heads) over an E4M3 cache
+    # holding codes of the N(0,1) pool / 0.02; the step's tokens quantised by the call.
+    from paged_kv_attention_03_gb300.inputs import make_case
+    case = make_case("varlen_prefill", seed=0, device=cuda)
+    s = 0.02
+    kc, vc = _codes_of(case.k_cache, s), _codes_of(case.v_cache, s)
+    _fp8_prefill_check(case, kc, vc, s, cuda, fused_store=True,
+                       what="full size varlen_prefill over an FP8 cache")

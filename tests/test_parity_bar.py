@@ -54,3 +54,18 @@ def test_bar_rejects_mean_error():
     got = ref + 2e-3  # every element within max-abs, the mean far off
     with pytest.raises(AssertionError):
         assert_parity(_bf16(got), ref)
+
+
+def test_mean_bar_ignores_only_the_output_rounding():
+    # Rows equal to single V values of an FP8 cache (code * 0.02) are not bf16 numbers: the
+    # correctly rounded output differs from them by ~1e-3 on average, which passes; the same
+    # rows shifted by 1.5e-3 do not.
+    codes = np.random.default_rng(3).standard_normal(8192) / 0.02
+    ref = np.round(codes) * 0.02
+    st = assert_parity(_bf16(round_to(ref, torch.bfloat16)), ref)
+    assert st["mean_abs"] > 5e-4 and st["mean_abs_vs_rounded"] == 0.0
+    # A bias of 1.5e-3 on rows of magnitude < 0.25 (bf16 spacing <= 2^-10) fails the mean bar
+    # while every element stays within max-abs.
+    small = ref * 0.1
+    with pytest.raises(AssertionError, match="mean-abs"):
+        assert_parity(_bf16(small + 1.5e-3), small)
