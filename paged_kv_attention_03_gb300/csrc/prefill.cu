@@ -1333,8 +1333,12 @@ void plan_prefix_splits(int num_req, int num_heads, int num_kv_heads, int prefix
     const int q_items = (num_req + 2 * tok - 1) / (2 * tok);
     const int tiles = (prefix_len + BN - 1) / BN;
     const int per_split = q_items * num_kv_heads;
-    // Enough key splits that the items cover every SM once, at least one tile each.
-    int want = (sm_count() + per_split - 1) / (per_split > 0 ? per_split : 1);
+    // About one prefix item per 8 SMs (at least one tile each): the prefix is little work
+    // (each page is read once for all requests), and the suffix decode, which reads every
+    // request's own keys, runs beside it on the SMs the prefix leaves free.  Over 64
+    // requests sharing 4096 keys: 0.045 ms against 0.052 (one item per 16 SMs) and 0.057
+    // (one per SM).
+    int want = (sm_count() / 8 + per_split - 1) / (per_split > 0 ? per_split : 1);
     if (want < 1) want = 1;
     if (want > tiles) want = tiles;
     const int chunk = tiles > 0 ? (tiles + want - 1) / want : 1;

@@ -173,3 +173,54 @@ def test_dcp_decode_single_rank_is_plain_decode(cuda):
     out = dcp_decode(case.q, case.k_cache, case.v_cache, bt, L, int(case.seq_lens.max()),
                      case.workload.final_scale)
     assert_parity(out, oracle_attention(case, host_inputs(case)), "dcp x1")
+
+
+@pytest.mark.parametrize("deal", ["contiguous", "interleave16", "interleave64"])
+@pytest.mark.parametrize("window", [1, 100, 1500, 5000])
+def test_context_parallel_decode_with_window(cuda, deal, window):
+    # Ranks emulated on one GPU as above, each with its own local cache; the window is on
+    # global positions, so each rank starts at its first visible local key.
+    from paged_kv_attention_03_gb300.dcp import dcp_key_begin
+
+    ranks = 3
+    w = Workload("dcpw", 32, 8, 128, 16, ())
+    lens = np.array([700, 4096, 33, 2001, 1])
+    case = make_case_from_lengths(w, list(lens - 1), [1] * len(lens), seed=86, device=cuda)
+    bs = w.block_size
+    inter = 0 if deal == "contiguous" else int(deal[len("interleave"):])
+    states, lses = [], []
+    for r in range(ranks):
+        if inter:
+            owned = [np.nonzero((np.arange(L) // inter) % ranks == r)[0] for L in lens]
+            starts = None
+        else:
+            st_, en_ = (lens * r) // ranks, (lens * (r + 1)) // ranks
+            owned = [np.arange(a, b) for a, b in zip(st_, en_)]
+            starts = torch.as_tensor(st_.astype(np.int32), device=cuda)
+        local_len = np.array([len(o) for o in owned], dtype=np.int32)
+        nblk = (local_len + bs - 1) // bs
+        pool_k = torch.zeros(int(nblk.sum()) + 1, bs, w.num_kv_heads, w.head_dim,
+                             dtype=torch.bfloat16, device=cuda)
+        pool_v = torch.zeros_like(pool_k)
+        table = np.full((len(lens), max(1, int(nblk.max()))), -1, dtype=np.int32)
+        nxt = 0
+        for b in range(len(lens)):
+            for j, pos in enumerate(owned[b]):
+                if j % bs == 0:
+                    table[b, j // bs] = nxt
+                    nxt += 1
+                src_blk = int(case.block_table[b, pos // bs])
+                pool_k[int(table[b, j // bs]), j % bs] = case.k_cache[src_blk, pos % bs]
+                pool_v[int(table[b, j // bs]), j % bs] = case.v_cache[src_blk, pos % bs]
+        kb = dcp_key_begin(_t(lens, cuda), window, r, ranks, inter, starts, _t(local_len, cuda))
+        # the rule, written out: keys of this rank with global position < L - window
+        want = [int(np.sum(o < max(0, L - window))) for o, L in zip(owned, lens)]
+        assert kb.cpu().tolist() == want
+        s, l = pa.pa_decode_state(case.q, pool_k, pool_v, _t(table, cuda), _t(local_len, cuda),
+                                  max(1, int(local_len.max())), w.final_scale, key_begin=kb)
+        states.append(s)
+        lses.append(l)
+    assert pa.pa_read_device_error(device=cuda) == 0
+    out = pa.pa_merge_states(torch.stack(states), torch.stack(lses))
+    assert_parity(out, oracle_attention(case, host_inputs(case), window=window),
+                  f"dcp {deal} window {window}")

@@ -112,3 +112,30 @@ def test_context_parallel_exchange_two_ranks():
                                              own_lses.reshape(2, -1).astype(np.float64))
     np.testing.assert_allclose(merged[0], own_states[0, 0, 0], rtol=0, atol=1e-6)
     assert merged_lse[0] == pytest.approx(float(own_lses[0, 0, 0]), abs=1e-6)
+
+
+@pytest.mark.parametrize("interleave", [0, 1, 16, 64])
+def test_dcp_key_begin_counts_the_keys_before_the_window(interleave):
+    # CPU: each rank's first visible local key is the number of its keys whose global
+    # position lies before the window (brute force over the deal).
+    import numpy as np
+    import torch
+    from paged_kv_attention_03_gb300.dcp import dcp_key_begin
+
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 5000, size=40).astype(np.int32)
+    world = 3
+    for window in (1, 7, 100, 4999, 6000):
+        for r in range(world):
+            if interleave:
+                owned = [np.nonzero((np.arange(L) // interleave) % world == r)[0] for L in lens]
+                starts = None
+            else:
+                st = (lens.astype(np.int64) * r) // world
+                en = (lens.astype(np.int64) * (r + 1)) // world
+                owned = [np.arange(a, b) for a, b in zip(st, en)]
+                starts = torch.as_tensor(st.astype(np.int32))
+            nloc = torch.as_tensor(np.array([len(o) for o in owned], dtype=np.int32))
+            kb = dcp_key_begin(torch.as_tensor(lens), window, r, world, interleave, starts, nloc)
+            want = [int(np.sum(o < max(0, int(L) - window))) for o, L in zip(owned, lens)]
+            assert kb.tolist() == want, (interleave, window, r)
