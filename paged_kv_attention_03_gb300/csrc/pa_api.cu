@@ -496,7 +496,16 @@ pa_status varlen_prefill(void *out, const void *q, const void *key, const void *
     if (num_blocks * block_size > 0x7fffff00LL || total_q > 0x7fffff00) return PA_ERR_UNSUPPORTED;
     const bool has_new = key || value || slot_mapping;
     if (has_new && !(key && value && slot_mapping)) return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    if (total_q == 0) return PA_OK;
+    // With no sequence there is nothing to attend, but the new tokens are still stored.
+    auto store = [&]() -> pa_status {
+        return fp8 ? pa_store_kvcache_fp8(key, value, k_cache, v_cache, slot_mapping, total_q,
+                                          num_blocks, block_size, num_kv_heads, head_dim, kv_scale,
+                                          stream)
+                   : pa_store_kvcache(key, value, k_cache, v_cache, slot_mapping, total_q,
+                                      num_blocks, block_size, num_kv_heads, head_dim, stream);
+    };
+    if (num_seqs == 0) return has_new ? store() : PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_table || !cu_seqlens_q) return PA_ERR_INVALID_ARG;
     if (!seq_lens && !cu_seqlens_k) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -504,12 +513,7 @@ pa_status varlen_prefill(void *out, const void *q, const void *key, const void *
     if (max_seqlen_k > 0 && max_num_blocks == 0) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (has_new) {
-        const pa_status st = fp8 ? pa_store_kvcache_fp8(key, value, k_cache, v_cache, slot_mapping,
-                                                        total_q, num_blocks, block_size,
-                                                        num_kv_heads, head_dim, kv_scale, stream)
-                                 : pa_store_kvcache(key, value, k_cache, v_cache, slot_mapping,
-                                                    total_q, num_blocks, block_size,
-                                                    num_kv_heads, head_dim, stream);
+        const pa_status st = store();
         if (st != PA_OK) return st;
     }
     pa::PrefillArgs a{};

@@ -147,15 +147,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-// Copy a 128-row x 256-bit matrix from shared memory (matrix descriptor s_desc, the
-// operand layout an MMA reads) to tensor memory: row r -> lane r, its 32 bytes -> the 8
-// columns from taddr.  Asynchronous; it runs in issue order with this thread's later
-// tcgen05.mma, and a later tcgen05.commit tracks its completion.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc)
-                 : "memory");
-}
-
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_03_gb300 as pa
 from paged_kv_attention_03_gb300.inputs import Workload, bf16_bits, make_case_from_lengths
 
@@ -95,6 +96,64 @@ def test_prefill_with_store_overwrites_stale_new_rows(cuda):
     out = _prefill(case, m, True)
     assert pa.pa_read_device_error(device=cuda) == 0
     assert_parity(out, ref)
+    np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
+
+
+@pytest.mark.parametrize("H,Hkv,D", [(8, 8, 64), (16, 16, 128)])
+def test_prefill_fused_store_group_one_spans_three_tiles(cuda, H, Hkv, D):
+    # G = 1: a work item is 256 query tokens, whose new keys reach over three 128-key tiles
+    # (with a context of 7 the first and last only partly).
+    w = Workload("g1", H, Hkv, D, 16, ())
+    case = make_case_from_lengths(w, [7, 200, 0], [300, 257, 129], seed=80, device=cuda)
+    other = _twin(case)
+    m = device_tensors(case, cuda)
+    fused = _prefill(case, m, True)
+    assert pa.pa_read_device_error(device=cuda) == 0
+    sep = _prefill(other, m, False)
+    assert torch.equal(fused, sep)
+    assert torch.equal(case.k_cache, other.k_cache)
+    assert torch.equal(case.v_cache, other.v_cache)
+    assert_parity(fused, oracle_attention(case, host_inputs(other)))
+
+
+def test_prefill_fused_store_writes_rows_no_sequence_owns(cuda):
+    # Rows of key / value before cu_seqlens_q[0] and from cu_seqlens_q[num_seqs] on belong
+    # to no sequence: the store still writes those with a slot (and skips slot -1).
+    w = Workload("fo", 8, 2, 128, 16, ())
+    nb = 64
+    case = make_case_from_lengths(w, [5, 40], [30, 70], seed=79, device=cuda, num_blocks=nb)
+    used = set(case.block_table[case.block_table >= 0].ravel().tolist())
+    free = [b for b in range(nb) if b not in used]
+    front = [free[0] * 16 + 1, -1, free[0] * 16 + 7]
+    back = [free[1] * 16, free[1] * 16 + 15, -1, free[2] * 16 + 3]
+    g = torch.Generator(device=cuda).manual_seed(5)
+    rnd = lambda n, heads: torch.randn(n, heads, 128, generator=g, device=cuda).to(torch.bfloat16)
+    q = torch.cat([rnd(3, 8), case.q, rnd(4, 8)])
+    key = torch.cat([rnd(3, 2), case.key, rnd(4, 2)])
+    value = torch.cat([rnd(3, 2), case.value, rnd(4, 2)])
+    slots = np.concatenate([front, case.slot_mapping, back]).astype(np.int32)
+    h = host_inputs(case)
+    oracle.store_kvcache(bf16_bits(key), bf16_bits(value), h["k_cache"], h["v_cache"], slots, 16)
+    ref = oracle_attention(case, h)
+    m = device_tensors(case, cuda)
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a), dtype=torch.int32, device=cuda)
+    out = pa.pa_varlen_prefill(q, case.k_cache, case.v_cache, t(case.cu_seqlens_q + 3),
+                               m["seq_lens"], m["block_table"], case.max_query_len,
+                               case.max_seq_len, w.final_scale, 0, key=key, value=value,
+                               slot_mapping=t(slots))
+    assert pa.pa_read_device_error(device=cuda) == 0
+    np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
+    np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
+    assert_parity(out[3:3 + int(case.cu_seqlens_q[-1])], ref)
+    # No sequence at all: nothing is attended, the rows are still stored.
+    key2, value2 = rnd(2, 2), rnd(2, 2)
+    slots2 = np.array([free[3] * 16 + 2, free[3] * 16 + 9], np.int32)
+    oracle.store_kvcache(bf16_bits(key2), bf16_bits(value2), h["k_cache"], h["v_cache"], slots2, 16)
+    pa.pa_varlen_prefill(rnd(2, 8), case.k_cache, case.v_cache, t([0]), t([]),
+                         torch.zeros((0, 1), dtype=torch.int32, device=cuda), 0, 0,
+                         w.final_scale, 0, key=key2, value=value2, slot_mapping=t(slots2))
+    assert pa.pa_read_device_error(device=cuda) == 0
     np.testing.assert_array_equal(bf16_bits(case.k_cache), h["k_cache"])
     np.testing.assert_array_equal(bf16_bits(case.v_cache), h["v_cache"])
 
