@@ -66,12 +66,15 @@ class L2Flush:
 # captures summarised in the named profiles/ files (commands there), with the commit of
 # the kernel source they were taken on.  A changed kernel needs a new capture.
 NCU_TRAFFIC = {
-    "decode_split_kernel": {"bytes": 639.53e6 + 3.92e6,
+    "decode_split_kernel": {"bytes": 639.59e6 + 4.18e6,
                             "source": "profiles/decode_split_kernel_batched_decode.md",
-                            "kernel_commit": "4a9b103"},
-    "prefill_kernel": {"bytes": 316.23e6 + 104.09e6,
+                            "kernel_commit": "87584a3"},
+    "decode_split_kernel_long": {"bytes": 2934.96e6 + 3.58e6,
+                                 "source": "profiles/decode_split_kernel_long_decode.md",
+                                 "kernel_commit": "87584a3"},
+    "prefill_kernel": {"bytes": 318.82e6 + 104.83e6,
                        "source": "profiles/prefill_kernel_varlen_prefill.md",
-                       "kernel_commit": "4a9b103"},
+                       "kernel_commit": "87584a3"},
 }
 
 
@@ -802,7 +805,11 @@ def _long_decode_leg(pa, dev, rank, peaks, flush, stream, args):
             "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_split_kernel + combine)",
                          "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(ach / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"]},
+                         "peak_source": peaks["source"],
+                         "traffic": NCU_TRAFFIC["decode_split_kernel_long"]["bytes"],
+                         "traffic_kernel": "decode_split_kernel",
+                         "traffic_source": NCU_TRAFFIC["decode_split_kernel_long"],
+                         "algorithmic_bytes": runner.work},
             "clocks": clocks}
 
 
