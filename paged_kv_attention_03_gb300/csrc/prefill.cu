@@ -468,9 +468,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// One 128-key tile of E4M3 codes, [128 rows][128 codes] row-major in the upper half of a
-// stage, expanded in place into the f16 operand layout of the stage ([128][64] per 64-dim
-// half, 128-byte swizzle), by one whole warp (4 rows a lane).  A row's f16 output of its
+// One 128-key tile of E4M3 codes, [128 rows][128 codes] in the upper half of a stage with
+// the 128-byte swizzle (16-byte chunk j of row r at r * 128 + ((j ^ r) & 7) * 16, so the
+// lanes' reads of one chunk index hit 8 different bank groups), expanded in place into the
+// f16 operand layout of the stage ([128][64] per 64-dim half, 128-byte swizzle), by one
+// whole warp (4 rows a lane).  A row's f16 output of its
 // upper half shares its 128-byte line with the row's own codes only, and the lane reads
 // all of them before it writes, so no lane overwrites codes another lane still needs.
 __device__ __forceinline__ void convert_tile_e4m3(uint32_t stage, int lane) {
@@ -480,7 +482,7 @@ __device__ __forceinline__ void convert_tile_e4m3(uint32_t stage, int lane) {
         const uint32_t r = static_cast<uint32_t>(lane + 32 * i);
         uint4 c[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) c[j] = ld_shared_v4(stage + kCodes + r * 128u + j * 16u);
+        for (int j = 0; j < 8; ++j) c[j] = ld_shared_v4(stage + kCodes + r * 128u + ((j ^ (r & 7u)) << 4));
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             // codes of head dims 16 j .. 16 j + 15: 64-dim half j / 4, 16-byte chunks 2 (j % 4)
@@ -675,47 +677,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                // The codes of tile t land in the upper half of its stage (barrier B_LK / B_LV);
-                // the warp converts tile t - (NS - 1) once tile t is issued, so NS - 1 tiles of
-                // codes are in flight while it converts, and converts what is pending while
-                // the next item is not yet published.
+                // The codes of tile t land in the upper half of its stage (barrier B_LK / B_LV)
+                // and are expanded there to f16.  The warp polls and does whichever step is
+                // ready: take the next item, issue the next tile's codes once its stage is
+                // free, expand the oldest tile whose codes have landed.  So a tile is expanded
+                // as soon as it lands, while the tensor core still reads the tile before it,
+                // and no issue waits behind an expansion it does not need.
                 constexpr int b_land = is_k ? B_LK : B_LV;
-                uint32_t tc = 0;  // tiles converted
-                auto convert_next = [&]() -> bool {
-                    const uint32_t st = tc % NS;
-                    if (!wait_warp(bar(b_land + st), (tc / NS) & 1, abort_flag, p.err, p.wait_ns))
-                        return false;
-                    convert_tile_e4m3(sbase + st * L::TILE, lane);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(b_full + st));
-                    ++tc;
-                    return true;
-                };
-                for (uint32_t ic = 0; ok; ++ic) {
-                    while (ok && tc < t &&
-                           !__all_sync(0xffffffffu, mbar_test_wait(bar(B_IFULL + ic % kRing), (ic / kRing) & 1)))
-                        ok = convert_next();
-                    if (!ok || !take_item(ic, it)) break;
-                    for (int j = 0; j < it.n_tiles; ++j) {
+                uint32_t tc = 0;  // tiles expanded
+                uint32_t ic = 0;  // items taken
+                int j = 0;
+                bool have = false, done = false;
+                uint64_t idle0 = 0;  // start of the current idle spell (0: none)
+                for (uint32_t spin = 0; ok;) {
+                    if (!have && !done &&
+                        __all_sync(0xffffffffu, mbar_test_wait(bar(B_IFULL + ic % kRing), (ic / kRing) & 1))) {
+                        if (take_item(ic, it)) {
+                            have = it.n_tiles > 0;
+                            j = 0;
+                        } else {
+                            done = true;
+                        }
+                        ++ic;
+                        idle0 = 0;
+                        continue;
+                    }
+                    if (have) {
                         const uint32_t st = t % NS;
-                        if (t >= NS && !wait_warp(bar(b_empty + st), ((t / NS) - 1) & 1, abort_flag,
-                                                  p.err, p.wait_ns)) {
+                        if (t < NS ||
+                            __all_sync(0xffffffffu, mbar_test_wait(bar(b_empty + st), ((t / NS) - 1) & 1))) {
+                            if (lane == 0) mbar_arrive_expect_tx(bar(b_land + st), L::TILE / 2);
+                            __syncwarp();
+                            if (lane < BN / 16) {  // one 16-key piece of codes per lane
+                                const int row = kv_row(it, (it.kt0 + j) * BN + 16 * lane);
+                                tma_load_3d(sbase + st * L::TILE + L::TILE / 2 + lane * 2048, map, 0,
+                                            it.kvh, row, bar(b_land + st));
+                            }
+                            ++t;
+                            if (++j == it.n_tiles) have = false;
+                            idle0 = 0;
+                            continue;
+                        }
+                    }
+                    if (tc < t) {
+                        const uint32_t sc = tc % NS;
+                        if (__all_sync(0xffffffffu, mbar_test_wait(bar(b_land + sc), (tc / NS) & 1))) {
+                            convert_tile_e4m3(sbase + sc * L::TILE, lane);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(b_full + sc));
+                            ++tc;
+                            idle0 = 0;
+                            continue;
+                        }
+                    }
+                    if (done && tc == t) break;
+                    // Nothing ready: bounded like every wait.
+                    if ((++spin & 31u) == 0) {
+                        const uint64_t now = globaltimer_ns();
+                        if (idle0 == 0) idle0 = now;
+                        const bool stop = *abort_flag != 0 || now - idle0 > p.wait_ns;
+                        if (__any_sync(0xffffffffu, stop)) {
+                            if (lane == 0) {
+                                *abort_flag = 1;
+                                flag_error(p.err, kErrTimeout);
+                            }
                             ok = false;
-                            break;
                         }
-                        if (lane == 0) mbar_arrive_expect_tx(bar(b_land + st), L::TILE / 2);
-                        __syncwarp();
-                        if (lane < BN / 16) {  // one 16-key piece of codes per lane
-                            const int row = kv_row(it, (it.kt0 + j) * BN + 16 * lane);
-                            tma_load_3d(sbase + st * L::TILE + L::TILE / 2 + lane * 2048, map, 0, it.kvh,
-                                        row, bar(b_land + st));
-                        }
-                        ++t;
-                        while (ok && t - tc > NS - 1) ok = convert_next();
                     }
                 }
-                while (ok && tc < t) ok = convert_next();
             }
             };
             if (warp == kWarpK)
@@ -1183,11 +1213,10 @@ bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uin
     const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    // codes: one-byte FP8 codes, rows copied as they are (no swizzle)
+    // codes: one-byte FP8 codes (128-byte rows, swizzled like the bf16 halves)
     const CUresult r = fn(map, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
