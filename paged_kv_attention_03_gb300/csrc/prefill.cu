@@ -883,7 +883,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (end) break;
             if constexpr (FP8) {
                 // The item's query tiles to f16, in place (a thread converts its row; the
-                // 16-byte chunks of a row share its 128-byte line whatever the swizzle).  Both
+                // 16-byte chunks of a row share its 128-byte line whatever the swizzle, and
+                // taking them in swizzled order puts the 8 rows of a lane octet on 8 bank
+                // groups).  Both
                 // warpgroups wait for the item's Q load even when tile 1 has no rows, so
                 // neither arrives on QCONV for a later item before this one's phase is done.
                 if (!wait_warp(bar(B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) break;
@@ -893,7 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < NHALF; ++h)
 #pragma unroll
                             for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint32_t a = sQ + wg * L::TILE + h * HALF + row * 128 + c8 * 16;
+                                const uint32_t a = sQ + wg * L::TILE + h * HALF + row * 128 +
+                                                   ((c8 ^ (row & 7)) << 4);
                                 const uint4 v = ld_shared_v4(a);
                                 st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                              bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
