@@ -195,3 +195,23 @@ def test_fp8_prefill_full_size_varlen(cuda):
     kc, vc = _codes_of(case.k_cache, s), _codes_of(case.v_cache, s)
     _fp8_prefill_check(case, kc, vc, s, cuda, fused_store=True,
                        what="full size varlen_prefill over an FP8 cache")
+
+
+def test_fp8_prefill_wait_limit_runs_out_then_device_is_usable(cuda):
+    # The FP8 K / V producers poll instead of waiting on one barrier; with the testing aid
+    # (no work item handed out) their idle spell and every other role's wait run out after
+    # 20 ms, the launch flags PA_DEVERR_TIMEOUT and returns, and the next call is correct.
+    case, kc, vc, s = _fp8_prefill_case(cuda, [0, 30], [200, 64], seed=116)
+    w = case.workload
+    pa.pa_read_device_error(clear=True, device=cuda)
+    pa.pa_debug_prefill_stall(True, 20_000_000)
+    try:
+        pa.pa_varlen_prefill_fp8(case.q, torch.from_numpy(kc).to(cuda),
+                                 torch.from_numpy(vc).to(cuda), _t(case.cu_seqlens_q, cuda),
+                                 _t(case.seq_lens, cuda), _t(case.block_table, cuda),
+                                 case.max_query_len, case.max_seq_len, w.final_scale, s, 0)
+        flags = pa.pa_read_device_error(clear=True, device=cuda)
+    finally:
+        pa.pa_debug_prefill_stall(False, 0)
+    assert flags & pa.DEVERR_TIMEOUT, f"flags {flags:#x}"
+    _fp8_prefill_check(case, kc, vc, s, cuda, what="FP8 prefill after a timed-out launch")
