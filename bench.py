@@ -547,9 +547,12 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-tiny", action="store_true")
-    ap.add_argument("--leg", default="both", choices=["both", "decode", "prefill"],
-                    help="decode: the decode step only; prefill: the prefill step only "
-                         "(profiling runs); both: the full JSON line")
+    ap.add_argument("--leg", default="both",
+                    choices=["both", "decode", "prefill", "fp8_decode", "fp8_prefill", "cascade",
+                             "mixed"],
+                    help="one leg alone, printing its JSON object (profiling runs): decode, "
+                         "prefill, fp8_decode, fp8_prefill, cascade or mixed; both: the full "
+                         "JSON line")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     rank, local, ws = _dist()
@@ -564,9 +567,18 @@ def main():
     pa.build()
     pa.load()
     peaks = _peaks()
-    if args.leg == "prefill":
+    if args.leg in ("prefill", "fp8_prefill", "cascade", "mixed", "fp8_decode"):
         flush = L2Flush(dev)
-        res = _prefill_leg(pa, dev, rank, peaks, flush, torch.cuda.current_stream(dev), args)
+        stream = torch.cuda.current_stream(dev)
+        if args.leg == "fp8_decode":
+            # The batched-decode batch over an E4M3 cache, as in the full line.
+            case = make_case(WORKLOADS["batched_decode"], seed=rank, device=dev)
+            res = _fp8_leg(pa, dev, rank, peaks, flush, stream, args, case,
+                           DecodeRunner(case, dev))
+        else:
+            leg = {"prefill": _prefill_leg, "fp8_prefill": _fp8_prefill_leg,
+                   "cascade": _cascade_leg, "mixed": _mixed_leg}[args.leg]
+            res = leg(pa, dev, rank, peaks, flush, stream, args)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
