@@ -727,6 +727,22 @@ __global__ void __launch_bounds__(NWARPS * 32, (decode_ctas_per_sm<FP8, NT>())) 
     }
 }
 
+// acc += w * (one lane's 16- or 8-byte slice of a partial fp32 row).
+template <int N>
+__device__ __forceinline__ void add_row_slice(float (&acc)[N], const float *src, float w) {
+    if constexpr (N == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+    }
+}
+
 // Log-sum-exp merge of the splits of one (sequence, head) per warp:
 //   M = max_s m_s,  w_s = l_s * 2^(m_s - M),  out = sum_s w_s O_s / sum_s w_s
 // where O_s are the normalised split outputs.
@@ -734,15 +750,19 @@ template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelParams p,
                                                              int batch) {
     constexpr int PER_LANE = D / 32;
-    sm100::griddep_wait();  // launched early (programmatic serialization): the splits must be done
+    static_assert(PER_LANE == 4 || PER_LANE == 2, "16- or 8-byte row slices");
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int b = gw / p.num_heads;
     const int h = gw - b * p.num_heads;
-    if (b >= batch) return;
+    if (b >= batch) {
+        sm100::griddep_wait();
+        return;
+    }
+    // The call's own inputs (not written by the split grid) are read before the wait.
     const SeqRange sr = decode_range(p.seq_lens[b], p.seq_cap, p.window,
-                                     p.key_begin ? p.key_begin[b] : p.key_begin_all, p.err,
-                                     false);
+                                     p.key_begin ? p.key_begin[b] : p.key_begin_all, p.err, false);
+    sm100::griddep_wait();  // launched early (programmatic serialization): the splits must be done
     const int nsplit = sr.L > sr.start ? (sr.L - sr.base + p.chunk - 1) / p.chunk : 0;
     const int64_t bh = static_cast<int64_t>(b) * p.num_heads + h;
     __nv_bfloat16 *dst = p.out + bh * D + lane * PER_LANE;
@@ -761,17 +781,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
     }
     const float *ml = p.ws_ml + bh * p.num_splits * 2;
     const float *os = p.ws_o + bh * p.num_splits * D + lane * PER_LANE;
-    // Split s's (m, l) live in lane s % 32; one round trip for all of them.
+    // Split s's (m, l) and extra part r's lse (log2 of its softmax mass is lse / ln 2) live in
+    // lanes s % 32 and r % 32; both are loaded in one round trip when there are at most 32.
     float M = -INFINITY;
-    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    for (int s0 = 0; s0 < nsplit || s0 < npre; s0 += 32) {
         const int s = s0 + lane;
         const float m = s < nsplit ? ml[2 * s] : -INFINITY;
-        M = fmaxf(M, m);
-    }
-    // Extra parts: log2 of their softmax mass is lse / ln 2.
-    for (int r0 = 0; r0 < npre; r0 += 32) {
-        const int r = r0 + lane;
-        M = fmaxf(M, r < npre ? p.pre_lse[r * pre_rows + bh] * kLog2e : -INFINITY);
+        const float e = s < npre ? p.pre_lse[s * pre_rows + bh] * kLog2e : -INFINITY;
+        M = fmaxf(M, fmaxf(m, e));
     }
     M = warp_max(M);
     if (M == -INFINITY) M = 0.f;  // every part empty: all weights are 0
@@ -786,33 +803,19 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeKernelP
         const int n = min(32, nsplit - s0);
         // The partial rows of these splits, four loads in flight per lane.
 #pragma unroll 4
-        for (int k = 0; k < n; ++k) {
-            const float w = __shfl_sync(0xffffffffu, wl, k);
-            const float *src = os + static_cast<int64_t>(s0 + k) * D;
-            if constexpr (PER_LANE == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-                acc[2] += w * v.z;
-                acc[3] += w * v.w;
-            } else {
-#pragma unroll
-                for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
-            }
-        }
+        for (int k = 0; k < n; ++k)
+            add_row_slice<PER_LANE>(acc, os + static_cast<int64_t>(s0 + k) * D,
+                                    __shfl_sync(0xffffffffu, wl, k));
     }
     for (int r0 = 0; r0 < npre; r0 += 32) {
         const int r = r0 + lane;
         const float wl = r < npre ? ex2_approx(p.pre_lse[r * pre_rows + bh] * kLog2e - M) : 0.f;
         wsum += wl;
         const int n = min(32, npre - r0);
-        for (int k = 0; k < n; ++k) {
-            const float w = __shfl_sync(0xffffffffu, wl, k);
-            const float *src = p.pre_o + (static_cast<int64_t>(r0 + k) * pre_rows + bh) * D +
-                               lane * PER_LANE;
-#pragma unroll
-            for (int i = 0; i < PER_LANE; ++i) acc[i] += w * src[i];
-        }
+        for (int k = 0; k < n; ++k)
+            add_row_slice<PER_LANE>(
+                acc, p.pre_o + (static_cast<int64_t>(r0 + k) * pre_rows + bh) * D + lane * PER_LANE,
+                __shfl_sync(0xffffffffu, wl, k));
     }
     wsum = warp_sum(wsum);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
