@@ -90,11 +90,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // Two bf16 (low half first) -> two f16: exact for values in the f16 normal range, rounded
-// below it, clamped to +-65504 beyond it.
+// below it, clamped to +-65504 beyond it (one saturating conversion; a NaN stays NaN).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
-    const float hi = fminf(fmaxf(__uint_as_float(w & 0xffff0000u), -65504.f), 65504.f);
-    return pack_f16x2(lo, hi);
+    uint32_t h;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(h)
+        : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+    return h;
 }
 
 // lo += float(f16 low half of v), hi += float(f16 high half of v) (mixed-precision adds).

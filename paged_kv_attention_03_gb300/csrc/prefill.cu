@@ -885,9 +885,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The item's query tiles to f16, in place (a thread converts its row; the
                 // 16-byte chunks of a row share its 128-byte line whatever the swizzle, and
                 // taking them in swizzled order puts the 8 rows of a lane octet on 8 bank
-                // groups).  Both
-                // warpgroups wait for the item's Q load even when tile 1 has no rows, so
-                // neither arrives on QCONV for a later item before this one's phase is done.
+                // groups).  Both warpgroups wait for the item's Q load even when tile 1 has no
+                // rows, so neither arrives on QCONV for a later item before this one's phase
+                // is done.
                 if (!wait_warp(bar(B_QFULL), ic & 1, abort_flag, p.err, p.wait_ns)) break;
                 if (wg == 0 || it.has1) {
                     if (row_in_tile) {
