@@ -107,3 +107,49 @@ def test_store_on_a_side_stream(cuda):
     hkv, d = case.key.shape[1], case.key.shape[2]
     assert torch.equal(k_snap.view(-1, hkv, d)[slots].view(torch.int16), case.key.view(torch.int16))
     assert torch.equal(v_snap.view(-1, hkv, d)[slots].view(torch.int16), case.value.view(torch.int16))
+
+
+def test_two_calls_on_two_streams_at_once(cuda):
+    # A mixed varlen call (its decode launch runs beside the prefill kernel) and a split-K
+    # decode with its own workspace, queued on two streams that run at the same time: no
+    # state is shared between calls but the device error word.
+    wp = Workload("tp", 32, 8, 128, 16, ())
+    cp = make_case_from_lengths(wp, [0, 5, 300, 1000], [200, 1, 129, 1], seed=96, device=cuda)
+    mp = device_tensors(cp, cuda)
+    wd = Workload("td", 32, 8, 128, 16, ())
+    cd = make_case_from_lengths(wd, [15, 700, 2047, 3000, 4000], [1] * 5, seed=97, device=cuda)
+    md = device_tensors(cd, cuda)
+    max_len = int(cd.seq_lens.max())
+    ws = torch.empty(max(pa.pa_decode_workspace_size(5, 32, 8, 128, max_len, 0, 0), 1),
+                     dtype=torch.uint8, device=cuda)
+
+    def prefill(dst):
+        pa.pa_varlen_prefill(cp.q, cp.k_cache, cp.v_cache, mp["cu_seqlens_q"], mp["seq_lens"],
+                             mp["block_table"], cp.max_query_len, cp.max_seq_len,
+                             wp.final_scale, 0, key=cp.key, value=cp.value,
+                             slot_mapping=mp["slot_mapping"], out=dst)
+
+    def decode(dst):
+        pa.pa_decode(cd.q, cd.k_cache, cd.v_cache, md["block_table"], md["seq_lens"], max_len,
+                     wd.final_scale, 0, 0, key=cd.key, value=cd.value,
+                     slot_mapping=md["slot_mapping"], out=dst, workspace=ws)
+
+    out_p, out_d = torch.empty_like(cp.q), torch.empty_like(cd.q)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            prefill(out_p)
+        with torch.cuda.stream(s2):
+            decode(out_d)
+    for s in (s1, s2):
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref_p, ref_d = torch.empty_like(out_p), torch.empty_like(out_d)
+    prefill(ref_p)
+    decode(ref_d)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error(device=cuda) == 0
+    assert torch.equal(out_p, ref_p)
+    assert torch.equal(out_d, ref_d)
