@@ -904,8 +904,8 @@ def _fp8_prefill_leg(pa, dev, rank, peaks, flush, stream, args):
 
 
 def _prefill_leg(pa, dev, rank, peaks, flush, stream, args):
-    """TFLOP/s of the varlen causal prefill workload (store + prefill), or None if the
-    prefill entry point is not available in this build."""
+    """TFLOP/s of the varlen causal prefill workload (store + prefill), or a status entry
+    if the library's prefill entry point returns an error."""
     case = make_case(WORKLOADS["varlen_prefill"], seed=100 + rank, device=dev)
     runner = PrefillRunner(case, dev)
     try:

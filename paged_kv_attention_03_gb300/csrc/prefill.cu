@@ -1111,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 8; ++k)
                             a[c][k] = pack_bf16x2(o[c >> 1][(c & 1) * 16 + 2 * k] * inv,
                                                   o[c >> 1][(c & 1) * 16 + 2 * k + 1] * inv);
-                    // Round 1 (partner j ^ 2): bb[r1][b] = (row (j & 1) | 2 r1, slice (j & 2) | b)
+                    // Exchange 1 (partner j ^ 2): bb[r1][b] = (row (j & 1) | 2 r1, slice (j & 2) | b)
                     uint32_t bb[2][2][8];
 #pragma unroll
                     for (int b = 0; b < 2; ++b)
@@ -1122,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bb[0][b][k] = b1 ? recv : a[b][k];
                             bb[1][b][k] = b1 ? a[2 | b][k] : recv;
                         }
-                    // Round 2 (partner j ^ 1): f[r] = (row r, slice j)
+                    // Exchange 2 (partner j ^ 1): f[r] = (row r, slice j)
                     uint32_t f[4][8];
 #pragma unroll
                     for (int r1 = 0; r1 < 2; ++r1)
