@@ -163,8 +163,8 @@ pa_status pa_decode(void *out, const void *q, const void *key, const void *value
                     void *stream);
 
 /*
- * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory.  The
- * paper has no counterpart: this is a calling convention of this library only.
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory.  No page
+ * the library follows defines it: this is a calling convention of this library only.
  *
  * Some callers have no way to call cudaMalloc: a plugin whose host framework hands it
  * just the tensors of the call and owns every other byte of the GPU, a binding from a
