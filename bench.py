@@ -207,6 +207,17 @@ def prefill_flops(case, seqs=None):
     return attended_keys(case, seqs) * 4 * w.head_dim * w.num_heads
 
 
+def cascade_bytes(case, prefix_len):
+    """(logical, physical) K+V bytes of a shared-prefix decode batch: logical counts every
+    request's keys (what plain decode reads), physical each cache row once (the prefix
+    rows are shared by all requests, each suffix is its request's own)."""
+    w = case.workload
+    row = w.num_kv_heads * w.head_dim * 2 * 2  # K + V bytes of one key
+    logical = int(case.seq_lens.sum()) * row
+    physical = (prefix_len + int((case.seq_lens - prefix_len).sum())) * row
+    return logical, physical
+
+
 # ------------------------------------------------------------------ runners ---
 
 class DecodeRunner:
@@ -402,9 +413,7 @@ class CascadeRunner:
                               dtype=torch.uint8, device=device)
         need = pa.pa_decode_workspace_size(64, 32, 8, 128, self.max_len, 0, 0)
         self.dws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-        row = w.num_kv_heads * w.head_dim * 2 * 2  # K + V bytes of one key
-        self.logical_bytes = int(c.seq_lens.sum()) * row
-        self.physical_bytes = (self.prefix + int(suffix.sum())) * row
+        self.logical_bytes, self.physical_bytes = cascade_bytes(c, self.prefix)
 
     def cascade(self):
         c = self.case

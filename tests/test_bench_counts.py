@@ -60,3 +60,21 @@ def test_prefill_flops_count_every_multiply_add():
                     if m[r, j]:
                         flops += 2 * w.head_dim + 2 * w.head_dim
     assert bench.prefill_flops(case) == flops
+
+
+def test_cascade_physical_bytes_count_each_cache_row_once():
+    # Requests sharing the first 4 blocks of their tables: the physical bytes are the
+    # distinct cache rows their keys reach through the block table, counted once each.
+    from paged_kv_attention_03_gb300.inputs import make_shared_prefix_case
+
+    w = Workload("cas", 8, 2, 64, 16, ())
+    prefix_blocks = 4
+    case = make_shared_prefix_case(w, prefix_blocks, [5, 20, 1, 33], seed=6, device="cpu")
+    rows = set()
+    for b, L in enumerate(case.seq_lens):
+        for j in range(int(L)):
+            rows.add((int(case.block_table[b, j // w.block_size]), j % w.block_size))
+    row_bytes = w.num_kv_heads * w.head_dim * 2 * 2
+    logical, physical = bench.cascade_bytes(case, prefix_blocks * w.block_size)
+    assert physical == len(rows) * row_bytes
+    assert logical == int(case.seq_lens.sum()) * row_bytes
